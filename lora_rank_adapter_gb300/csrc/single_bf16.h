@@ -1,0 +1,76 @@
+// single_bf16.h -- argument structs and launchers shared by the single-adapter
+// kernels and the C ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/lora.h"
+
+namespace lora {
+
+// Validated arguments of one single-adapter call (forward roles, strides in elements).
+struct SingleArgs {
+  lora_dtype_t dtype;
+  int64_t M, K, L;
+  int r;
+  const void *X; int64_t ldx;
+  const void *A; int64_t sA_k, sA_r;
+  const void *B; int64_t sB_r, sB_l;
+  void *Y; int64_t ldy;
+  const void *dY; int64_t lddy;
+  void *dX; int64_t lddx;
+  float *dA; int64_t sdA_k, sdA_r;
+  float *dB; int64_t sdB_r, sdB_l;
+  float scale;
+};
+
+// Whether A / B are repacked into the workspace, and the row strides used.
+struct SingleLayout {
+  bool pack_A = false, pack_B = false;
+  int64_t lda = 0, ldb = 0;
+};
+
+struct FwdArgs {
+  int M, K, L;
+  float scale;
+  int cl;
+};
+
+struct RowsArgs {
+  int M, Kc, csplit;
+  float *part;
+  int *counters;
+  int ncounters;
+};
+
+struct ColArgs {
+  int M, K, r, cp, msplit, nkb;   // for dB, K holds L and nkb the number of 64-column blocks of L
+  float scale;
+  float *part_out;
+  int *counters;
+  float *out;
+  int64_t out_s0, out_s1;
+};
+
+SingleLayout plan_layout(const SingleArgs &a, bool need_A, bool need_B);
+size_t bf16_ws_bytes(int op, int64_t M, int64_t K, int64_t L, int r);
+size_t f32_ws_bytes(int op, int64_t M, int64_t K, int64_t L, int r);
+
+lora_status_t forward_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
+lora_status_t backward_dx_da_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
+lora_status_t backward_db_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
+
+lora_status_t forward_f32(const SingleArgs &a, cudaStream_t st);
+lora_status_t backward_dx_da_f32(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
+lora_status_t backward_db_f32(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
+
+// Zero fills used for degenerate shapes (outputs defined as overwritten).
+lora_status_t fill_zero_2d(lora_dtype_t dt, void *p, int64_t rows, int64_t cols, int64_t s_row, int64_t s_col,
+                           cudaStream_t st);
+
+int read_clear_error_single_bf16();
+int read_clear_error_single_f32();
+
+}  // namespace lora

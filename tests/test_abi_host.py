@@ -1,0 +1,110 @@
+"""The C ABI library on the host: it loads, exports every declared entry point,
+and rejects bad arguments before launching anything (no GPU needed)."""
+import ctypes
+
+import pytest
+
+from lora_rank_adapter_gb300 import _build
+from lora_rank_adapter_gb300 import binding as B
+from tests._util import header_functions
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return B.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    declared = header_functions()
+    assert len(declared) == 12, declared
+    assert sorted(B.EXPORTS) == declared
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(L):
+    assert L.lora_version().decode().startswith("lora-gb300")
+    for code, name in B.STATUS.items():
+        assert L.lora_status_string(code).decode().startswith(name)
+
+
+FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: every call below fails validation
+MIS = ctypes.c_void_p(0x10002)       # not 16-byte aligned
+NULL = ctypes.c_void_p(0)
+S0 = ctypes.c_void_p(0)
+
+
+def fwd(L, dt=1, M=64, K=64, L_=64, r=16, X=FAKE, ldx=64, A=FAKE, sak=1, sar=64, Bp=FAKE, sbr=1, sbl=16,
+        Y=FAKE, ldy=64, ws=NULL, wsb=0):
+    return L.lora_forward(dt, M, K, L_, r, X, ldx, A, sak, sar, Bp, sbr, sbl, Y, ldy, 1.0, ws, wsb, S0)
+
+
+def test_forward_argument_errors(L):
+    assert fwd(L, dt=7) == 2                       # unsupported dtype
+    assert fwd(L, M=-1) == 1
+    assert fwd(L, r=-1) == 1
+    assert fwd(L, r=129) == 2                      # rank above LORA_MAX_RANK
+    assert fwd(L, X=NULL) == 1
+    assert fwd(L, Y=NULL) == 1
+    assert fwd(L, A=NULL) == 1
+    assert fwd(L, X=MIS) == 3                      # misaligned big operand
+    assert fwd(L, ldx=60) == 1                     # ldx < K
+    assert fwd(L, ldx=68) == 3                     # row stride not a 16-byte multiple (bf16)
+    assert fwd(L, dt=0, ldx=66, K=66) == 3         # fp32: 264 bytes is not a multiple of 16
+    # A stored K x r (not the TMA-readable layout) needs workspace for repacking
+    assert fwd(L, sak=16, sar=1) == 4
+    # degenerate shapes are a no-op and touch nothing (no device needed)
+    assert fwd(L, M=0, X=NULL, Y=NULL) == 0
+    assert fwd(L, r=0, A=NULL, Bp=NULL) == 0
+    assert fwd(L, K=0) == 0
+
+
+def test_backward_argument_errors(L):
+    dx = lambda **k: L.lora_backward_dx_da(k.get("dt", 1), k.get("M", 64), 64, 64, k.get("r", 16),
+                                           k.get("X", FAKE), 64, k.get("dY", FAKE), 64, FAKE, 1, 64,
+                                           FAKE, 1, 16, 1.0, k.get("dX", FAKE), 64, k.get("dA", FAKE), 16, 1,
+                                           k.get("ws", NULL), k.get("wsb", 0), S0)
+    assert dx(dt=3) == 2
+    assert dx(r=1000) == 2
+    assert dx(dX=NULL) == 1
+    assert dx(dA=NULL) == 1
+    assert dx(dY=MIS) == 3
+    assert dx() == 4                               # the backward always needs workspace
+    need = L.lora_workspace_size(B.OP_BACKWARD_DX_DA, 1, 64, 64, 64, 16, 0)
+    assert need > 0
+    assert dx(ws=ctypes.c_void_p(0x10080), wsb=need) == 4     # not 256-byte aligned
+    assert dx(ws=ctypes.c_void_p(0x10000), wsb=need - 1) == 4  # too small
+    db = lambda **k: L.lora_backward_db(1, 64, 64, 64, 16, k.get("X", FAKE), 64, FAKE, 1, 64, FAKE, 64, 1.0,
+                                        k.get("dB", FAKE), 64, 1, NULL, 0, S0)
+    assert db(dB=NULL) == 1
+    assert db(X=MIS) == 3
+    assert db() == 4
+
+
+def test_workspace_sizes_monotone(L):
+    for op in (B.OP_FORWARD, B.OP_BACKWARD_DX_DA, B.OP_BACKWARD_DB):
+        small = L.lora_workspace_size(op, 1, 256, 512, 512, 8, 0)
+        big = L.lora_workspace_size(op, 1, 8192, 4096, 4096, 16, 0)
+        assert big >= small >= 0
+        assert L.lora_workspace_size(op, 1, 256, 512, 512, 500, 0) == 0   # invalid rank
+    assert L.lora_workspace_size(B.OP_BACKWARD_DX_DA, 0, 256, 512, 512, 8, 0) == 256 * 8 * 4
+
+
+def test_multi_argument_errors(L):
+    slots = ctypes.c_void_p(0x20000)
+    ad = B.LoraAddressing(slots.value, 16, 4, 8)
+    P = ctypes.byref
+    osl = (ctypes.c_int32 * 1)(32)
+    assert L.lora_shrink(None, FAKE, 64, 1, FAKE, 64, FAKE, 512, 64, FAKE, 8, NULL, 0, S0) == 1
+    bad = B.LoraAddressing(slots.value, 16, 0, 8)
+    assert L.lora_shrink(P(bad), FAKE, 64, 1, FAKE, 64, FAKE, 512, 64, FAKE, 8, NULL, 0, S0) == 1
+    bad = B.LoraAddressing(slots.value, 16, 5000, 8)
+    assert L.lora_shrink(P(bad), FAKE, 64, 1, FAKE, 64, FAKE, 512, 64, FAKE, 8, NULL, 0, S0) == 2
+    assert L.lora_shrink(P(ad), FAKE, 64, 9, FAKE, 64, FAKE, 512, 64, FAKE, 72, NULL, 0, S0) == 2
+    assert L.lora_shrink(P(ad), FAKE, 64, 1, MIS, 64, FAKE, 512, 64, FAKE, 8, NULL, 0, S0) == 3
+    assert L.lora_expand(P(ad), FAKE, FAKE, None, 1, FAKE, 8, FAKE, 256, 8, 1, FAKE, 32, NULL, 0, S0) == 1
+    assert L.lora_expand(P(ad), FAKE, NULL, osl, 1, FAKE, 8, FAKE, 256, 8, 1, FAKE, 32, NULL, 0, S0) == 1
+    assert L.lora_gather_shrink(P(ad), FAKE, 100, NULL, FAKE, 800, 100, 1, FAKE, 8, S0) == 1
+    empty = B.LoraAddressing(0, 0, 4, 8)
+    assert L.lora_gather_shrink(P(empty), NULL, 100, NULL, NULL, 800, 100, 1, NULL, 8, S0) == 0
