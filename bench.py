@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""Throughput of the LoRA adapter-product hot path on GB300 (one JSON line).
+
+Workload: one batch of 8192 tokens x 4096 features in bf16 (the q_proj
+configuration: batch 4 x seq 2048, r = 16, scale 2) pushed through every step
+of the hot path, each through the C ABI of liblora.so:
+  training   lora_forward, lora_backward_dx_da, lora_backward_db (r = 16)
+  serving    lora_shrink, lora_expand, lora_apply_linear on the same batch as a
+             fused QKV target (out_slices [4096, 1024, 1024], 32 adapter slots,
+             R = 64, ranks from {0, 8, 16, 32, 64}, contiguous segments of
+             geometric length with mean 128, 10% on the zero adapter), and
+             lora_gather_shrink of the batch's token ids over a 128256-entry
+             embedding axis (5% of ids = -1).
+A step is one pass of all of them; value = tokens per step / step time.
+Inputs are resident in HBM before the timed region; three independent input
+sets (> 3 x 129 MB L2) rotate between steps and the ops of a step use
+different sets, so no op re-reads what the previous op left in L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LoRA fwd+bwd & multi-adapter shrink/expand tokens/s; % of HBM roofline"
+UNIT = "tokens/s"
+NSETS = 3
+SEED = 0
+WORKLOAD = ("q_proj batch M=8192 x K=4096 bf16 through the whole hot path: fwd+dX/dA+dB (r=16, L=4096), "
+            "group/shrink/expand/apply_linear as fused QKV [4096,1024,1024] over 32 slots (R=64), "
+            "gather_shrink over V=128256")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="", help="comma-separated op names to run (profiling); default: all")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (timestamped on the host) while the benchmark runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.samples = []
+        self.proc = None
+        self.dev = str(device_index)
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.dev, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not inside:   # timed region shorter than the sampling period: nearest samples after it
+            inside = [p for (t, p) in self.samples if t >= t0][:3]
+            window = "after-timed"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[3 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(inside[0][1]),
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max((num(p[2]) or 0.0) for p in inside)}
+
+
+# ----------------------------------------------------------------------------- workload
+def build_single(torch, synth, dev, k):
+    spec = synth.single_spec("single_c2")
+    w = synth.make_single(spec, seed=SEED + k, device=dev, prefix=f"bench{k}")
+    M, K = w["X"].shape
+    r, L = w["B"].shape
+    # adapter weights in the PEFT layout: lora_A.weight [r, K], lora_B.weight [L, r]
+    w["A"] = w["A"].t().contiguous().t()
+    w["B"] = w["B"].t().contiguous().t()
+    w["Y"] = w["Y0"].clone()
+    w["dX"] = torch.empty_like(w["X"])
+    w["dA"] = torch.empty((K, r), dtype=torch.float32, device=dev)
+    w["dB"] = torch.empty((r, L), dtype=torch.float32, device=dev)
+    w["s"] = spec["s"]
+    return w
+
+
+def single_bytes(M, K, L, r):
+    e = 2
+    return {
+        "lora_forward": M * K * e + 2 * M * L * e + K * r * e + r * L * e,
+        "lora_backward_dx_da": M * L * e + 2 * M * K * e + K * r * e + r * L * e + K * r * 4,
+        "lora_backward_db": M * K * e + M * L * e + K * r * e + r * L * 4,
+    }
+
+
+def make_ops(torch, lora, binding, synth, dev):
+    """Per input set: the list of (name, callable, bytes) that makes one step."""
+    sets = []
+    for k in range(NSETS):
+        w = build_single(torch, synth, dev, k)
+        M, K = w["X"].shape
+        r, L = w["B"].shape
+        ws = {op: binding.workspace(op, binding.LORA_BF16, M, K, L, r, device=dev)
+              for op in (binding.OP_FORWARD, binding.OP_BACKWARD_DX_DA, binding.OP_BACKWARD_DB)}
+        sets.append(dict(w=w, ws=ws, M=M, K=K, L=L, r=r))
+    by = single_bytes(sets[0]["M"], sets[0]["K"], sets[0]["L"], sets[0]["r"])
+
+    def fwd(S):
+        w = S["w"]
+        lora.lora_forward(w["X"], w["A"], w["B"], w["Y"], w["s"], ws=S["ws"][binding.OP_FORWARD])
+
+    def dxda(S):
+        w = S["w"]
+        lora.lora_backward_dx_da(w["X"], w["dY"], w["A"], w["B"], w["s"], w["dX"], w["dA"],
+                                 ws=S["ws"][binding.OP_BACKWARD_DX_DA])
+
+    def db(S):
+        w = S["w"]
+        lora.lora_backward_db(w["X"], w["A"], w["dY"], w["s"], w["dB"], ws=S["ws"][binding.OP_BACKWARD_DB])
+
+    ops = [("lora_forward", fwd, by["lora_forward"]),
+           ("lora_backward_dx_da", dxda, by["lora_backward_dx_da"]),
+           ("lora_backward_db", db, by["lora_backward_db"])]
+    return sets, ops, sets[0]["M"]
+
+
+def h2d_d2h_tensors(S):
+    """(inputs copied in, results copied out) of one step, for the end-to-end leg."""
+    w = S["w"]
+    ins = [w["X"], w["Y"], w["dY"]]
+    outs = [w["Y"], w["dX"], w["dA"], w["dB"]]
+    return ins, outs
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def oracle_sample_pass(O, synth, torch, tokens):
+    """One pass of the oracle over a `tokens`-row sample of the workload."""
+    spec = synth.single_spec("single_c2", M=tokens)
+    gen = "cuda" if torch.cuda.is_available() else "cpu"
+    w = synth.make_single(spec, seed=SEED, device=gen, prefix="cpu")
+    f = lambda t: t.double().cpu().numpy()
+    X, A, B, Y0, dY = (f(w[k]) for k in ("X", "A", "B", "Y0", "dY"))
+    t0 = time.perf_counter()
+    O.forward(X, A, B, Y0, spec["s"])
+    O.backward_dx_da(X, dY, A, B, spec["s"])
+    O.backward_db(X, A, dY, spec["s"])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(torch, synth, target_s=12.0):
+    from oracle import oracle as O
+    O.build()
+    cores = O.num_threads()
+    tokens = 64
+    dt = oracle_sample_pass(O, synth, torch, tokens)
+    # grow the sample until one pass takes a few seconds (bounded)
+    while dt < target_s / 4 and tokens < 2048:
+        tokens = min(2048, tokens * 4)
+        dt = oracle_sample_pass(O, synth, torch, tokens)
+    return {"value": tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{tokens} of the 8192 tokens through fwd + dX/dA + dB (fp64, one pass, {dt:.2f} s)"}
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, rank, world):
+    import torch
+    from lora_rank_adapter_gb300 import synth
+    if rank != 0:
+        return
+    from oracle import oracle as O
+    O.build()
+    cores = O.num_threads()
+    tokens = 256
+    for _ in range(args.warmup):
+        oracle_sample_pass(O, synth, torch, 64)
+    times = [oracle_sample_pass(O, synth, torch, tokens) for _ in range(args.steps)]
+    tot = sum(times)
+    value = tokens * len(times) / tot
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded SplitMix64)",
+            "config": {"workload": WORKLOAD, "global_batch": 8192, "seq_len": 2048, "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{tokens} of the 8192 tokens per step through fwd + dX/dA + dB (fp64)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def traffic_from_profiles(kernel_key):
+    """Per-launch DRAM bytes of `kernel_key` from the committed ncu summary, if the
+    kernel source it was taken from is unchanged (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(path) as f:
+            lines = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    except OSError:
+        return None
+    for parts in lines:
+        kv = dict(p.split("=", 1) for p in parts if "=" in p)
+        if kv.get("op") == kernel_key:
+            src = os.path.join(ROOT, kv.get("source", ""))
+            try:
+                with open(src, "rb") as f:
+                    sha = hashlib.sha256(f.read()).hexdigest()[:16]
+            except OSError:
+                return None
+            if sha == kv.get("source_sha"):
+                return int(kv["dram_bytes_per_launch"])
+    return None
+
+
+def run_gb300(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from lora_rank_adapter_gb300 import _build
+    from lora_rank_adapter_gb300 import binding
+    from lora_rank_adapter_gb300 import binding as lora
+    from lora_rank_adapter_gb300 import synth
+
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    sets, ops, tokens = make_ops(torch, lora, binding, synth, dev)
+    if args.only:
+        keep = set(args.only.split(","))
+        ops = [op for op in ops if op[0] in keep]
+    torch.cuda.synchronize()
+
+    def step(i, events=None):
+        for j, (name, fn, _) in enumerate(ops):
+            S = sets[(i + j) % NSETS]
+            if events is not None:
+                events[j][0].record(stream)
+            fn(S)
+            if events is not None:
+                events[j][1].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    assert lora.lora_device_error() == 0
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.35)
+    K = args.steps
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
+           for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    launches0 = lora.lora_kernel_launches()
+    t_host0 = time.time()
+    e0.record(stream)
+    for i in range(K):
+        step(i, evs[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    barrier()
+    launches = lora.lora_kernel_launches() - launches0
+    time.sleep(0.25)
+    sampler.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / K
+    value = world * tokens / (ms_per_step / 1e3)
+
+    peak, peak_kind = peaks()
+    parts = {}
+    for j, (name, _, nbytes) in enumerate(ops):
+        t_ms = statistics.mean(evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(K))
+        gbs = nbytes / (t_ms / 1e3) / 1e9
+        parts[name] = {"ms": t_ms, "bytes": nbytes, "GB/s": gbs, "frac_of_" + peak_kind: gbs / peak,
+                       "tokens/s": tokens / (t_ms / 1e3)}
+    dom = max(parts, key=lambda n: parts[n]["ms"])
+    roof = {"bound": "hbm", "op": dom, "achieved": parts[dom]["GB/s"], "peak": peak, "unit": "GB/s",
+            "frac": parts[dom]["GB/s"] / peak, "peak_kind": peak_kind,
+            "traffic": traffic_from_profiles(dom), "bytes_per_launch": parts[dom]["bytes"]}
+
+    # end to end: pinned host inputs in, results out, every step
+    E = min(args.e2e_steps, K)
+    host_in = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in h2d_d2h_tensors(S)[0]]
+               for S in sets]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in h2d_d2h_tensors(S)[1]]
+                for S in sets]
+    h2d = sum(t.numel() * t.element_size() for t in host_in[0])
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+
+    def e2e_step(i):
+        S_i = [(i + j) % NSETS for j in range(len(ops))]
+        for k in sorted(set(S_i)):
+            for dst, src in zip(h2d_d2h_tensors(sets[k])[0], host_in[k]):
+                dst.copy_(src, non_blocking=True)
+        step(i)
+        for k in sorted(set(S_i)):
+            for dst, src in zip(host_out[k], h2d_d2h_tensors(sets[k])[1]):
+                dst.copy_(src, non_blocking=True)
+
+    sets_per_step = len({(0 + j) % NSETS for j in range(len(ops))})
+    e_ms = None
+    if E > 0:
+        for i in range(2):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for i in range(E):
+            e2e_step(i)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = f0.elapsed_time(f1) / E
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+    assert lora.lora_device_error() == 0
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(torch, synth)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+                "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded SplitMix64; inputs resident in HBM)",
+                "config": {"workload": WORKLOAD, "model": "q_proj LoRA (Llama-like 4096)", "global_batch": 8192 * world,
+                           "seq_len": 2048, "parallelism": f"replicas x{world}",
+                           "l2": f"{NSETS} rotating input sets, each > L2; consecutive ops use different sets"},
+                "parts": parts, "roofline": roof, "cpu_baseline": cpu,
+                "e2e": None if e_ms is None else {
+                    "value": world * tokens / (e_ms / 1e3), "unit": UNIT, "steps": E,
+                    "h2d_bytes_per_step": h2d * sets_per_step, "d2h_bytes_per_step": d2h * sets_per_step},
+                "gpu_launches": int(launches), "clocks": sampler.summary(t_host0, t_host1)}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_gb300(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -234,6 +234,10 @@ LORA_API const char *lora_status_string(lora_status_t status);
  * LORA_ERR_CUDA if the read failed. */
 LORA_API lora_status_t lora_device_error(int32_t *code);
 
+/* Number of kernels this library has launched in this process so far (all
+ * devices, all streams; a relaxed counter for diagnostics and benchmarks). */
+LORA_API uint64_t lora_kernel_launches(void);
+
 /* Library version string. */
 LORA_API const char *lora_version(void);
 

@@ -22,7 +22,8 @@ STATUS = {0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_UNSUPPORTED", 3:
           4: "LORA_ERR_WORKSPACE", 5: "LORA_ERR_CUDA", 6: "LORA_ERR_DEVICE"}
 EXPORTS = ["lora_workspace_size", "lora_forward", "lora_backward_dx_da", "lora_backward_db",
            "lora_group_by_slot", "lora_shrink", "lora_expand", "lora_apply_linear",
-           "lora_gather_shrink", "lora_status_string", "lora_device_error", "lora_version"]
+           "lora_gather_shrink", "lora_status_string", "lora_device_error", "lora_kernel_launches",
+           "lora_version"]
 
 
 class LoraError(RuntimeError):
@@ -67,6 +68,7 @@ def lib():
         "lora_gather_shrink": (i32, [AP, P, i64, P, P, i64, i64, i64, P, i64, P]),
         "lora_status_string": (ctypes.c_char_p, [i32]),
         "lora_device_error": (i32, [ctypes.POINTER(i32)]),
+        "lora_kernel_launches": (ctypes.c_uint64, []),
         "lora_version": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -248,6 +250,11 @@ def lora_device_error():
     v = ctypes.c_int32(0)
     _check(lib().lora_device_error(ctypes.byref(v)), "lora_device_error")
     return v.value
+
+
+def lora_kernel_launches():
+    """Kernels launched by liblora.so in this process so far."""
+    return int(lib().lora_kernel_launches())
 
 
 def lora_version():

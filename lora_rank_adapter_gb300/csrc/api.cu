@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -52,6 +53,9 @@ bool encode_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void 
 }
 
 static std::mutex g_mu;
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int num_sms() {
   static std::map<int, int> cache;
@@ -148,6 +152,8 @@ using namespace lora;
 extern "C" {
 
 const char *lora_version(void) { return "lora-gb300 0.1 (sm_103a)"; }
+
+uint64_t lora_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char *lora_status_string(lora_status_t s) {
   switch (s) {

@@ -58,6 +58,9 @@ struct WsCarver {
 };
 inline size_t ws_round(size_t b) { return (b + 255) & ~size_t(255); }
 
+// Counts every kernel launch issued through launch() (lora_kernel_launches()).
+void count_launch();
+
 // Launch with optional cluster dimension and programmatic dependent launch.
 template <typename... KArgs, typename... Args>
 cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster,
@@ -83,6 +86,7 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
   }
   cfg.attrs = attrs;
   cfg.numAttrs = n;
+  count_launch();
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

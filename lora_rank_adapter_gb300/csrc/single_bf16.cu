@@ -38,6 +38,17 @@ constexpr int NCW = 4;                  // consumer warps (one 16-row slice each
 constexpr int NTHREADS = (NCW + 1) * 32;
 constexpr int TILE_BYTES = BM * BK * 2; // 8 KB
 
+// Shared memory given to the stage ring of one CTA (bytes in flight per CTA);
+// the number of stages of each kernel follows from its stage size.
+#ifndef LORA_STAGE_BUDGET_KB
+#define LORA_STAGE_BUDGET_KB 48
+#endif
+__host__ __device__ constexpr int stages_for(int stage_bytes, int lo = 2, int hi = 16) {
+  return (LORA_STAGE_BUDGET_KB * 1024) / stage_bytes < lo   ? lo
+         : (LORA_STAGE_BUDGET_KB * 1024) / stage_bytes > hi ? hi
+                                                             : (LORA_STAGE_BUDGET_KB * 1024) / stage_bytes;
+}
+
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
@@ -87,28 +98,77 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
 }
 
 // =============================================================================
+// Warp roles shared by the kernels below: warps 0..3 consume (mma.sync), warp 4
+// loads (TMA), and in kernels that write tiles back, warp 5 stores (TMA).
+// Barriers per stage s: full[s] (loads landed, transaction count), done[s] (the
+// four consumer warps are finished with the stage) and, with a storer, free[s]
+// (the store has read the stage; the loader may refill it).
+// =============================================================================
+constexpr int NTHREADS_LS = (NCW + 2) * 32;   // consumers + loader + storer
+constexpr int kStoreDepth = 2;                // TMA stores kept in flight by the storer
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Storer loop (one lane).  For every tile g in order: wait until the consumers
+// are done with its stage, issue its TMA store if store(g, s) does so, and free
+// stages for the loader once their stores have read them.  At most D stores
+// stay unreleased; D < NS keeps a free stage for the loader, so the loader,
+// consumers and storer can always make progress.  Tiles without a store are
+// freed at once.
+template <int NS, typename StoreFn>
+__device__ __forceinline__ void storer_run(int ntiles, uint64_t *done, uint64_t *freeb, StoreFn store) {
+  static_assert(NS >= 2, "a storer needs at least two stages");
+  constexpr int D = (NS - 1) < kStoreDepth ? (NS - 1) : kStoreDepth;
+  int pend[D + 1];
+  int np = 0;
+  for (int g = 0; g < ntiles; ++g) {
+    const int s = g % NS;
+    if (!mbar_wait(&done[s], (g / NS) & 1)) break;
+    if (store(g, s)) {
+      bulk_commit();
+      pend[np++] = g;
+      if (np > D) {
+        bulk_wait_read<D>();
+        mbar_arrive(&freeb[pend[0] % NS]);
+        for (int i = 1; i < np; ++i) pend[i - 1] = pend[i];
+        --np;
+      }
+    } else {
+      mbar_arrive(&freeb[s]);
+    }
+  }
+  bulk_wait_read<0>();
+  for (int i = 0; i < np; ++i) mbar_arrive(&freeb[pend[i] % NS]);
+  bulk_wait_all();
+}
+
+// =============================================================================
 // Forward: Y[M,L] += s * (X*Ac^T) * Bc^T
 // A cluster of `cl` CTAs shares one 64-row block: CTA c runs K-chunks
 // [c*nk/cl, (c+1)*nk/cl) of the shrink, the partial h are summed in cluster-rank
 // order through distributed shared memory (identical in every CTA), then CTA c
 // runs its share of the L-chunks of the expand.  X is read once and Y is read
-// and written once.
+// and written once; Y tiles are updated in place in their stage and written
+// back by the storer warp.
 // =============================================================================
 template <int RP>
 struct FwdCfg {
   static constexpr int SMALL = RP * 128;          // Ac [RP][64] or Bc [64][RP]
   static constexpr int STAGE = TILE_BYTES + SMALL;
-  static constexpr int NS = RP <= 32 ? 6 : 4;
+  static constexpr int NS = stages_for(STAGE, 3);
   static constexpr int HBUF = BM * RP * 4;
-  static constexpr int BYTES = 1024 + NS * STAGE + HBUF + 8 * (2 * NS + 2);
+  static constexpr int BYTES = 1024 + NS * STAGE + HBUF + 8 * (3 * NS + 2);
 };
 
 template <int RP>
-__global__ void __launch_bounds__(NTHREADS) fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
-                                                            const __grid_constant__ CUtensorMap tmA,
-                                                            const __grid_constant__ CUtensorMap tmB,
-                                                            const __grid_constant__ CUtensorMap tmY,
-                                                            FwdArgs p) {
+__global__ void __launch_bounds__(NTHREADS_LS) fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                               const __grid_constant__ CUtensorMap tmA,
+                                                               const __grid_constant__ CUtensorMap tmB,
+                                                               const __grid_constant__ CUtensorMap tmY,
+                                                               FwdArgs p) {
   using C = FwdCfg<RP>;
   constexpr int NS = C::NS;
   constexpr int PW = RP < 64 ? RP : 64;
@@ -116,8 +176,9 @@ __global__ void __launch_bounds__(NTHREADS) fwd_bf16_kernel(const __grid_constan
   uint8_t *smem = align1024(smem_raw);
   float *hbuf = reinterpret_cast<float *>(smem + NS * C::STAGE);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * C::STAGE + C::HBUF);
-  uint64_t *empty = full + NS;
-  uint64_t *hready = empty + NS;
+  uint64_t *done = full + NS;
+  uint64_t *freeb = done + NS;
+  uint64_t *hready = freeb + NS;
   uint64_t *hdone = hready + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -127,11 +188,13 @@ __global__ void __launch_bounds__(NTHREADS) fwd_bf16_kernel(const __grid_constan
   const int nk = (p.K + BK - 1) / BK, nl = (p.L + BK - 1) / BK;
   const int k_beg = (int)((int64_t)nk * crank / cl), k_end = (int)((int64_t)nk * (crank + 1) / cl);
   const int l_beg = (int)((int64_t)nl * crank / cl), l_end = (int)((int64_t)nl * (crank + 1) / cl);
+  const int n1 = k_end - k_beg, ntiles = n1 + (l_end - l_beg);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NCW);
+      mbar_init(&done[s], NCW);
+      mbar_init(&freeb[s], 1);
     }
     mbar_init(hready, cl > 1 ? NCW * 32 * (cl - 1) : 1);
     mbar_init(hdone, cl > 1 ? NCW * 32 * (cl - 1) : 1);
@@ -141,58 +204,41 @@ __global__ void __launch_bounds__(NTHREADS) fwd_bf16_kernel(const __grid_constan
   pdl_wait();
 
   if (warp == NCW) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ loader
     if (lane == 0) {
       prefetch_tmap(&tmX);
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
       prefetch_tmap(&tmY);
-      int pend[NS];
-      for (int s = 0; s < NS; ++s) pend[s] = -1;
-      int g = 0;
-      bool ok = true;
-      auto acquire = [&](int s) -> bool {
-        if (g >= NS) {
-          if (!mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) return false;
-          if (pend[s] >= 0) {
-            tma_store_2d(&tmY, smem + s * C::STAGE, pend[s] * BK, m0);
-            bulk_commit();
-            bulk_wait_read_all();
-            pend[s] = -1;
-          }
-        }
-        return true;
-      };
-      for (int kc = k_beg; ok && kc < k_end; ++kc, ++g) {
+      for (int g = 0; g < ntiles; ++g) {
         const int s = g % NS;
-        if (!(ok = acquire(s))) break;
+        if (g >= NS && !mbar_wait(&freeb[s], ((g / NS) & 1) ^ 1)) break;
         uint8_t *st = smem + s * C::STAGE;
         mbar_arrive_expect_tx(&full[s], C::STAGE);
-        tma_load_2d(st, &tmX, &full[s], kc * BK, m0);
-        tma_load_2d(st + TILE_BYTES, &tmA, &full[s], kc * BK, 0);
-      }
-      for (int lc = l_beg; ok && lc < l_end; ++lc, ++g) {
-        const int s = g % NS;
-        if (!(ok = acquire(s))) break;
-        uint8_t *st = smem + s * C::STAGE;
-        mbar_arrive_expect_tx(&full[s], C::STAGE);
-        tma_load_2d(st, &tmY, &full[s], lc * BK, m0);
+        if (g < n1) {
+          const int kc = k_beg + g;
+          tma_load_2d(st, &tmX, &full[s], kc * BK, m0);
+          tma_load_2d(st + TILE_BYTES, &tmA, &full[s], kc * BK, 0);
+        } else {
+          const int lc = l_beg + g - n1;
+          tma_load_2d(st, &tmY, &full[s], lc * BK, m0);
 #pragma unroll
-        for (int pp = 0; pp < RP / PW; ++pp)
-          tma_load_2d(st + TILE_BYTES + pp * (64 * PW * 2), &tmB, &full[s], pp * PW, lc * BK);
-        pend[s] = lc;
+          for (int pp = 0; pp < RP / PW; ++pp)
+            tma_load_2d(st + TILE_BYTES + pp * (64 * PW * 2), &tmB, &full[s], pp * PW, lc * BK);
+        }
       }
-      // drain the stores still owed, oldest first
-      for (int gg = (g > NS ? g - NS : 0); ok && gg < g; ++gg) {
-        const int s = gg % NS;
-        if (pend[s] < 0) continue;
-        if (!(ok = mbar_wait(&empty[s], (gg / NS) & 1))) break;
-        tma_store_2d(&tmY, smem + s * C::STAGE, pend[s] * BK, m0);
-        bulk_commit();
-        pend[s] = -1;
-      }
-      bulk_wait_all();
     }
+    pdl_launch_dependents();
+    return;
+  }
+  if (warp == NCW + 1) {
+    // ------------------------------------------------------------ storer
+    if (lane == 0)
+      storer_run<NS>(ntiles, done, freeb, [&](int g, int s) {
+        if (g < n1) return false;
+        tma_store_2d(&tmY, smem + s * C::STAGE, (l_beg + g - n1) * BK, m0);
+        return true;
+      });
     pdl_launch_dependents();
     return;
   }
@@ -202,9 +248,9 @@ __global__ void __launch_bounds__(NTHREADS) fwd_bf16_kernel(const __grid_constan
   float hacc[RP / 8][4];
 #pragma unroll
   for (int i = 0; i < RP / 8; ++i) hacc[i][0] = hacc[i][1] = hacc[i][2] = hacc[i][3] = 0.f;
-  int g = 0;
   bool ok = true;
-  for (int kc = k_beg; kc < k_end; ++kc, ++g) {
+  int g = 0;
+  for (; g < n1; ++g) {
     const int s = g % NS;
     if (!(ok = wait_all(&full[s], (g / NS) & 1))) break;
     const uint32_t tb = smem_u32(smem + s * C::STAGE), sb = tb + TILE_BYTES;
@@ -221,7 +267,7 @@ __global__ void __launch_bounds__(NTHREADS) fwd_bf16_kernel(const __grid_constan
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if (lane == 0) mbar_arrive(&done[s]);
   }
 
   if (cl > 1) {
@@ -267,7 +313,7 @@ __global__ void __launch_bounds__(NTHREADS) fwd_bf16_kernel(const __grid_constan
     split_bf16(hacc[2 * q + 1][2], hacc[2 * q + 1][3], ahi[q][3], alo[q][3]);
   }
   const float scale = p.scale;
-  for (int lc = l_beg; ok && lc < l_end; ++lc, ++g) {
+  for (; ok && g < ntiles; ++g) {
     const int s = g % NS;
     if (!(ok = wait_all(&full[s], (g / NS) & 1))) break;
     uint8_t *st = smem + s * C::STAGE;
@@ -298,25 +344,47 @@ __global__ void __launch_bounds__(NTHREADS) fwd_bf16_kernel(const __grid_constan
     }
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if (lane == 0) mbar_arrive(&done[s]);
   }
   pdl_launch_dependents();
   if (cl > 1) wait_all<true>(hdone, 0);   // peers are done reading this CTA's hbuf
 }
 
 // =============================================================================
-// Row products: part[c][m][j] = sum over contraction chunk c of In[m][k] * W(k, j)
+// Row products: out[m][j] = sum over the contraction of In[m][k] * W(k, j)
 //   dyb: In = dY (M x L), W = Bc [l][j]  (kW_KN = true: the store is [k][n])
 //   h:   In = X  (M x K), W = Ac [j][k]  (kW_KN = false: the store is [n][k])
-// Grid: (row blocks) x csplit; block 0 also zeroes the column-pass counters.
+// A cluster of `csplit` CTAs splits the contraction of one 64-row block; the
+// partials are summed in cluster-rank order through distributed shared memory
+// and written once, already split into bf16 hi/lo and laid out as the column
+// pass reads them (a "blob" of 2 x 64 x RP bf16 per row block, lr_off order).
+// Block 0 also zeroes the column-pass counters.
 // =============================================================================
 template <int RP>
 struct RowsCfg {
   static constexpr int SMALL = RP * 128;
   static constexpr int STAGE = TILE_BYTES + SMALL;
-  static constexpr int NS = RP <= 32 ? 6 : 4;
-  static constexpr int BYTES = 1024 + NS * STAGE + 8 * 2 * NS;
+  static constexpr int NS = stages_for(STAGE);
+  static constexpr int HBUF = BM * RP * 4;
+  static constexpr int BYTES = 1024 + NS * STAGE + HBUF + 8 * (2 * NS + 2);
 };
+template <int RP>
+__host__ __device__ constexpr int blob_bytes() { return RP * 256; }   // hi + lo, 64 rows x RP bf16 each
+
+template <int RP>
+__device__ __forceinline__ void write_blob_rows(uint8_t *blob, int w, int gq, int cq, const float (&acc)[RP / 8][4]) {
+  uint8_t *bhi = blob, *blo = blob + RP * 128;
+#pragma unroll
+  for (int nt = 0; nt < RP / 8; ++nt)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t h, l;
+      split_bf16(acc[nt][2 * hf], acc[nt][2 * hf + 1], h, l);
+      const uint32_t o = lr_off<RP>(16 * w + gq + 8 * hf, nt * 8 + 2 * cq);
+      *reinterpret_cast<uint32_t *>(bhi + o) = h;
+      *reinterpret_cast<uint32_t *>(blo + o) = l;
+    }
+}
 
 template <int RP, bool kW_KN>
 __global__ void __launch_bounds__(NTHREADS) rows_bf16_kernel(const __grid_constant__ CUtensorMap tmIn,
@@ -327,12 +395,16 @@ __global__ void __launch_bounds__(NTHREADS) rows_bf16_kernel(const __grid_consta
   constexpr int PW = RP < 64 ? RP : 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * C::STAGE);
+  float *hbuf = reinterpret_cast<float *>(smem + NS * C::STAGE);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * C::STAGE + C::HBUF);
   uint64_t *empty = full + NS;
+  uint64_t *hready = empty + NS;
+  uint64_t *hdone = hready + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cs = p.csplit;
-  const int c = blockIdx.x % cs;
-  const int m0 = (blockIdx.x / cs) * BM;
+  const uint32_t c = cs > 1 ? cluster_ctarank() : 0u;
+  const int rb = blockIdx.x / cs;
+  const int m0 = rb * BM;
   const int nk = (p.Kc + BK - 1) / BK;
   const int k_beg = (int)((int64_t)nk * c / cs), k_end = (int)((int64_t)nk * (c + 1) / cs);
 
@@ -341,9 +413,11 @@ __global__ void __launch_bounds__(NTHREADS) rows_bf16_kernel(const __grid_consta
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], NCW);
     }
+    mbar_init(hready, cs > 1 ? NCW * 32 * (cs - 1) : 1);
+    mbar_init(hdone, cs > 1 ? NCW * 32 * (cs - 1) : 1);
     fence_barrier_init();
   }
-  __syncthreads();
+  if (cs > 1) cluster_sync_all(); else __syncthreads();
   pdl_wait();
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < p.ncounters; i += blockDim.x) p.counters[i] = 0;
@@ -399,76 +473,82 @@ __global__ void __launch_bounds__(NTHREADS) rows_bf16_kernel(const __grid_consta
     if (lane == 0) mbar_arrive(&empty[s]);
   }
   pdl_launch_dependents();
-  if (!ok) return;
-  float *part = p.part + (int64_t)c * p.M * RP;
-#pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    const int m = m0 + 16 * w + gq + 8 * hf;
-    if (m < p.M) {
-#pragma unroll
-      for (int nt = 0; nt < RP / 8; ++nt)
-        *reinterpret_cast<float2 *>(&part[(int64_t)m * RP + nt * 8 + 2 * cq]) =
-            make_float2(hacc[nt][2 * hf], hacc[nt][2 * hf + 1]);
-    }
+  uint8_t *blob = p.blob + (size_t)rb * blob_bytes<RP>();
+  if (cs == 1) {
+    if (ok) write_blob_rows<RP>(blob, w, gq, cq, hacc);
+    return;
   }
-}
-
-// Sum of the csplit fp32 partials of rows [m0, m0+64) (already in shared memory,
-// [c][64][RP]) -> bf16 hi/lo stores [64][RP] (lr_off layout).  Consumer threads only.
-template <int RP>
-__device__ __forceinline__ void stage_split(const float *parts, int cp, uint8_t *hi, uint8_t *lo) {
-  const int t = threadIdx.x;   // 0 .. 127
-  for (int e = t; e < 64 * RP / 2; e += NCW * 32) {
-    const int row = e / (RP / 2), col = (e % (RP / 2)) * 2;
-    float2 v = *reinterpret_cast<const float2 *>(&parts[row * RP + col]);
-    for (int c = 1; c < cp; ++c) {
-      float2 u = *reinterpret_cast<const float2 *>(&parts[(c * 64 + row) * RP + col]);
-      v.x += u.x;
-      v.y += u.y;
-    }
-    uint32_t h, l;
-    split_bf16(v.x, v.y, h, l);
-    const uint32_t o = lr_off<RP>(row, col);
-    *reinterpret_cast<uint32_t *>(hi + o) = h;
-    *reinterpret_cast<uint32_t *>(lo + o) = l;
+  const int r0 = 16 * w + gq;
+#pragma unroll
+  for (int nt = 0; nt < RP / 8; ++nt) {
+    *reinterpret_cast<float2 *>(&hbuf[r0 * RP + nt * 8 + 2 * cq]) = make_float2(hacc[nt][0], hacc[nt][1]);
+    *reinterpret_cast<float2 *>(&hbuf[(r0 + 8) * RP + nt * 8 + 2 * cq]) = make_float2(hacc[nt][2], hacc[nt][3]);
   }
+  for (int q = 0; q < cs; ++q)
+    if (q != (int)c) mbar_arrive_remote(hready, q);
+  if (!wait_all<true>(hready, 0)) ok = false;
+  if (ok && (w % cs) == (int)c) {
+    // this CTA reduces (and writes) the 16 rows of warp w
+#pragma unroll
+    for (int nt = 0; nt < RP / 8; ++nt) {
+      float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+      for (int q = 0; q < cs; ++q) {
+        float2 v0, v1;
+        if (q == (int)c) {
+          v0 = make_float2(hacc[nt][0], hacc[nt][1]);
+          v1 = make_float2(hacc[nt][2], hacc[nt][3]);
+        } else {
+          v0 = ld_dsmem_f2(&hbuf[r0 * RP + nt * 8 + 2 * cq], q);
+          v1 = ld_dsmem_f2(&hbuf[(r0 + 8) * RP + nt * 8 + 2 * cq], q);
+        }
+        s0.x += v0.x; s0.y += v0.y; s1.x += v1.x; s1.y += v1.y;
+      }
+      hacc[nt][0] = s0.x; hacc[nt][1] = s0.y; hacc[nt][2] = s1.x; hacc[nt][3] = s1.y;
+    }
+    write_blob_rows<RP>(blob, w, gq, cq, hacc);
+  }
+  for (int q = 0; q < cs; ++q)
+    if (q != (int)c) mbar_arrive_remote(hdone, q);
+  wait_all<true>(hdone, 0);
 }
 
 // =============================================================================
 // Column pass for dX and dA.  CTA (kb, ms) owns the 64 columns k0 = 64*kb of X
-// and dX and walks its share of the 64-row tiles:
-//   dX[m, k0..] = s * dyb[m, :] * Ac[:, k0..]^T   (written through the stage, TMA store)
-//   dA[k0.., :] += X[m, k0..]^T * dyb[m, :]       (fp32 in registers)
-// The dA partial of each CTA goes to the workspace; the last CTA of column block
-// kb (atomic ticket, no waiting) sums the msplit partials in order and writes dA.
+// and dX and walks its share of the 64-row tiles.  Per tile the four consumer
+// warps split the 64 x 64 tile into 2 x 2 quarters (m-half mh, k-half kh):
+//   dX[mh, kh]  = s * dyb[mh, :] * Ac[:, kh]^T   (written over the X quarter)
+//   dA[kh, :]  += X[mh, kh]^T * dyb[mh, :]       (fp32 in registers)
+// so every warp reads and writes only its own quarter and no barrier is needed;
+// dyb arrives as the row pass's hi/lo blob.  At the end the two m-halves of dA
+// are summed, the CTA's partial goes to the workspace, and the last CTA of the
+// column block (atomic ticket, no waiting) sums the msplit partials in order
+// and writes dA.
 // =============================================================================
 template <int RP>
 struct ColCfg {
-  static constexpr int NS = RP <= 32 ? 4 : 3;
-  static constexpr int CPMAX = RP == 16 ? 4 : RP == 32 ? 2 : 1;
-  static constexpr int PARTS = CPMAX * 64 * RP * 4;
-  static constexpr int STAGE = TILE_BYTES + PARTS;
-  static constexpr int SPLIT = 64 * RP * 2;    // one bf16 [64][RP] buffer
+  static constexpr int BLOB = blob_bytes<RP>();
+  static constexpr int STAGE = TILE_BYTES + BLOB;
+  static constexpr int NS = stages_for(STAGE, 3, 8);
   static constexpr int SMALL = RP * 128;       // Ac tile
-  static constexpr int BYTES = 1024 + NS * STAGE + 2 * SPLIT + SMALL + 8 * (2 * NS + 1) + 16;
+  static constexpr int RED = 64 * RP * 4;      // cross-warp dA sum
+  static constexpr int BYTES = 1024 + NS * STAGE + SMALL + RED + 8 * (3 * NS + 1) + 16;
 };
 
 template <int RP>
-__global__ void __launch_bounds__(NTHREADS) colpass_dxda_kernel(const __grid_constant__ CUtensorMap tmX,
-                                                                const __grid_constant__ CUtensorMap tmA,
-                                                                const __grid_constant__ CUtensorMap tmDX,
-                                                                const __grid_constant__ CUtensorMap tmP,
-                                                                ColArgs p) {
+__global__ void __launch_bounds__(NTHREADS_LS) colpass_dxda_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                   const __grid_constant__ CUtensorMap tmA,
+                                                                   const __grid_constant__ CUtensorMap tmDX,
+                                                                   ColArgs p) {
   using C = ColCfg<RP>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  uint8_t *shi = smem + NS * C::STAGE;
-  uint8_t *slo = shi + C::SPLIT;
-  uint8_t *atile = slo + C::SPLIT;
-  uint64_t *full = reinterpret_cast<uint64_t *>(atile + C::SMALL);
-  uint64_t *empty = full + NS;
-  uint64_t *abar = empty + NS;
+  uint8_t *atile = smem + NS * C::STAGE;
+  float *red = reinterpret_cast<float *>(atile + C::SMALL);
+  uint64_t *full = reinterpret_cast<uint64_t *>(atile + C::SMALL + C::RED);
+  uint64_t *done = full + NS;
+  uint64_t *freeb = done + NS;
+  uint64_t *abar = freeb + NS;
   int *s_last = reinterpret_cast<int *>(abar + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -476,13 +556,13 @@ __global__ void __launch_bounds__(NTHREADS) colpass_dxda_kernel(const __grid_con
   const int k0 = kb * BK;
   const int nmt = (p.M + BM - 1) / BM;
   const int t_beg = (int)((int64_t)nmt * ms / p.msplit), t_end = (int)((int64_t)nmt * (ms + 1) / p.msplit);
-  const int cp = p.cp;
-  const uint32_t stage_bytes = TILE_BYTES + cp * 64 * RP * 4;
+  const int ntiles = t_end - t_beg;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NCW);
+      mbar_init(&done[s], NCW);
+      mbar_init(&freeb[s], 1);
     }
     mbar_init(abar, 1);
     fence_barrier_init();
@@ -495,120 +575,138 @@ __global__ void __launch_bounds__(NTHREADS) colpass_dxda_kernel(const __grid_con
       prefetch_tmap(&tmX);
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmDX);
-      prefetch_tmap(&tmP);
       mbar_arrive_expect_tx(abar, C::SMALL);
       tma_load_2d(atile, &tmA, abar, k0, 0);
-      int pend[NS];
-      for (int s = 0; s < NS; ++s) pend[s] = -1;
-      int g = 0;
-      bool ok = true;
-      for (int t = t_beg; t < t_end; ++t, ++g) {
+      for (int g = 0; g < ntiles; ++g) {
         const int s = g % NS;
+        if (g >= NS && !mbar_wait(&freeb[s], ((g / NS) & 1) ^ 1)) break;
         uint8_t *st = smem + s * C::STAGE;
-        if (g >= NS) {
-          if (!(ok = mbar_wait(&empty[s], ((g / NS) & 1) ^ 1))) break;
-          if (pend[s] >= 0) {
-            tma_store_2d(&tmDX, st, k0, pend[s]);
-            bulk_commit();
-            bulk_wait_read_all();
-            pend[s] = -1;
-          }
-        }
-        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        const int t = t_beg + g;
+        mbar_arrive_expect_tx(&full[s], C::STAGE);
         tma_load_2d(st, &tmX, &full[s], k0, t * BM);
-        tma_load_3d(st + TILE_BYTES, &tmP, &full[s], 0, t * BM, 0);
-        pend[s] = t * BM;
+        bulk_load(st + TILE_BYTES, p.blob + (size_t)t * C::BLOB, C::BLOB, &full[s]);
       }
-      for (int gg = (g > NS ? g - NS : 0); ok && gg < g; ++gg) {
-        const int s = gg % NS;
-        if (pend[s] < 0) continue;
-        if (!(ok = mbar_wait(&empty[s], (gg / NS) & 1))) break;
-        tma_store_2d(&tmDX, smem + s * C::STAGE, k0, pend[s]);
-        bulk_commit();
-        pend[s] = -1;
-      }
-      bulk_wait_all();
     }
+    pdl_launch_dependents();
+    return;
+  }
+  if (warp == NCW + 1) {
+    if (lane == 0)
+      storer_run<NS>(ntiles, done, freeb, [&](int g, int s) {
+        tma_store_2d(&tmDX, smem + s * C::STAGE, k0, (t_beg + g) * BM);
+        return true;
+      });
     pdl_launch_dependents();
     return;
   }
 
   const int w = warp, gq = lane >> 2, cq = lane & 3;
-  float dacc[RP / 8][4];
+  const int mh = w & 1, kh = w >> 1;
+  float dacc[2][RP / 8][4];
 #pragma unroll
-  for (int i = 0; i < RP / 8; ++i) dacc[i][0] = dacc[i][1] = dacc[i][2] = dacc[i][3] = 0.f;
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < RP / 8; ++j) dacc[i][j][0] = dacc[i][j][1] = dacc[i][j][2] = dacc[i][j][3] = 0.f;
   bool ok = wait_all(abar, 0);
-  const uint32_t ab = smem_u32(atile), hb = smem_u32(shi), lb = smem_u32(slo);
+  const uint32_t ab = smem_u32(atile);
   const float scale = p.scale;
-  int g = 0;
-  for (int t = t_beg; ok && t < t_end; ++t, ++g) {
+  for (int g = 0; ok && g < ntiles; ++g) {
     const int s = g % NS;
     if (!(ok = wait_all(&full[s], (g / NS) & 1))) break;
     uint8_t *st = smem + s * C::STAGE;
-    const uint32_t tb = smem_u32(st);
-    stage_split<RP>(reinterpret_cast<const float *>(st + TILE_BYTES), cp, shi, slo);
-    named_bar_sync(1, NCW * 32);
-    // dA rows k0 + 16w .. : contraction over the 64 rows of the tile
+    const uint32_t tb = smem_u32(st), bh = tb + TILE_BYTES, bl = bh + RP * 128;
+    // dA rows kh*32 + {0,16}: contraction over the 32 rows of this m-half
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t a[4];
-      ld_a_t(tb, 16 * w, kk * 16, tile_off, a);
+    for (int ks = 0; ks < 2; ++ks) {
+      const int mrow = mh * 32 + ks * 16;
+      uint32_t a[2][4];
+      ld_a_t(tb, kh * 32, mrow, tile_off, a[0]);
+      ld_a_t(tb, kh * 32 + 16, mrow, tile_off, a[1]);
 #pragma unroll
       for (int np = 0; np < RP / 16; ++np) {
-        uint32_t bh[4], bl[4];
-        ld_b_kn(hb, np * 16, kk * 16, lr_off<RP>, bh);
-        ld_b_kn(lb, np * 16, kk * 16, lr_off<RP>, bl);
-        mma_bf16(dacc[2 * np], a, bh[0], bh[1]);
-        mma_bf16(dacc[2 * np], a, bl[0], bl[1]);
-        mma_bf16(dacc[2 * np + 1], a, bh[2], bh[3]);
-        mma_bf16(dacc[2 * np + 1], a, bl[2], bl[3]);
+        uint32_t bhf[4], blf[4];
+        ld_b_kn(bh, np * 16, mrow, lr_off<RP>, bhf);
+        ld_b_kn(bl, np * 16, mrow, lr_off<RP>, blf);
+#pragma unroll
+        for (int kt = 0; kt < 2; ++kt) {
+          mma_bf16(dacc[kt][2 * np], a[kt], bhf[0], bhf[1]);
+          mma_bf16(dacc[kt][2 * np], a[kt], blf[0], blf[1]);
+          mma_bf16(dacc[kt][2 * np + 1], a[kt], bhf[2], bhf[3]);
+          mma_bf16(dacc[kt][2 * np + 1], a[kt], blf[2], blf[3]);
+        }
       }
     }
-    // dX rows 16w.. of the tile, 64 columns
-    float acc[8][4];
+    // dX rows mh*32 + {0,16}, columns kh*32 .. +32
+    float acc[2][4][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
 #pragma unroll
     for (int q = 0; q < RP / 16; ++q) {
-      uint32_t ah[4], al[4];
-      ld_a(hb, 16 * w, q * 16, lr_off<RP>, ah);
-      ld_a(lb, 16 * w, q * 16, lr_off<RP>, al);
+      uint32_t ah[2][4], al[2][4];
 #pragma unroll
-      for (int np = 0; np < 4; ++np) {
+      for (int mt = 0; mt < 2; ++mt) {
+        ld_a(bh, mh * 32 + mt * 16, q * 16, lr_off<RP>, ah[mt]);
+        ld_a(bl, mh * 32 + mt * 16, q * 16, lr_off<RP>, al[mt]);
+      }
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
         uint32_t b[4];
-        ld_b_kn(ab, np * 16, q * 16, rk_off, b);
-        mma_bf16(acc[2 * np], ah, b[0], b[1]);
-        mma_bf16(acc[2 * np], al, b[0], b[1]);
-        mma_bf16(acc[2 * np + 1], ah, b[2], b[3]);
-        mma_bf16(acc[2 * np + 1], al, b[2], b[3]);
+        ld_b_kn(ab, kh * 32 + np * 16, q * 16, rk_off, b);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          mma_bf16(acc[mt][2 * np], ah[mt], b[0], b[1]);
+          mma_bf16(acc[mt][2 * np], al[mt], b[0], b[1]);
+          mma_bf16(acc[mt][2 * np + 1], ah[mt], b[2], b[3]);
+          mma_bf16(acc[mt][2 * np + 1], al[mt], b[2], b[3]);
+        }
       }
     }
-    named_bar_sync(1, NCW * 32);   // every warp is done reading the X tile and the split buffers
+    __syncwarp();
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t *dp = reinterpret_cast<uint32_t *>(st + tile_off(16 * w + gq + 8 * hf, nt * 8 + 2 * cq));
-        *dp = pack_bf16(scale * acc[nt][2 * hf], scale * acc[nt][2 * hf + 1]);
-      }
-    }
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t *dp = reinterpret_cast<uint32_t *>(
+              st + tile_off(mh * 32 + mt * 16 + gq + 8 * hf, kh * 32 + nt * 8 + 2 * cq));
+          *dp = pack_bf16(scale * acc[mt][nt][2 * hf], scale * acc[mt][nt][2 * hf + 1]);
+        }
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if (lane == 0) mbar_arrive(&done[s]);
   }
   pdl_launch_dependents();
   if (!__all_sync(0xffffffffu, ok)) return;
 
-  // dA partial of this CTA, then the ordered reduction by the last CTA of the column block
+  // sum the two m-halves, write this CTA's partial, ordered reduction by the last CTA
+  if (mh == 1) {
+#pragma unroll
+    for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+      for (int nt = 0; nt < RP / 8; ++nt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+          *reinterpret_cast<float2 *>(&red[(kh * 32 + kt * 16 + gq + 8 * hf) * RP + nt * 8 + 2 * cq]) =
+              make_float2(dacc[kt][nt][2 * hf], dacc[kt][nt][2 * hf + 1]);
+  }
+  named_bar_sync(1, NCW * 32);
   const int64_t kpad = p.nkb * BK;
   float *part = p.part_out + (int64_t)ms * kpad * RP;
+  if (mh == 0) {
 #pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    const int k = k0 + 16 * w + gq + 8 * hf;
+    for (int kt = 0; kt < 2; ++kt)
 #pragma unroll
-    for (int nt = 0; nt < RP / 8; ++nt)
-      *reinterpret_cast<float2 *>(&part[(int64_t)k * RP + nt * 8 + 2 * cq]) =
-          make_float2(dacc[nt][2 * hf], dacc[nt][2 * hf + 1]);
+      for (int nt = 0; nt < RP / 8; ++nt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int kr = kh * 32 + kt * 16 + gq + 8 * hf;
+          const float2 o = *reinterpret_cast<const float2 *>(&red[kr * RP + nt * 8 + 2 * cq]);
+          *reinterpret_cast<float2 *>(&part[(int64_t)(k0 + kr) * RP + nt * 8 + 2 * cq]) =
+              make_float2(dacc[kt][nt][2 * hf] + o.x, dacc[kt][nt][2 * hf + 1] + o.y);
+        }
   }
   __threadfence();
   named_bar_sync(1, NCW * 32);
@@ -629,30 +727,33 @@ __global__ void __launch_bounds__(NTHREADS) colpass_dxda_kernel(const __grid_con
 
 // =============================================================================
 // Column pass for dB.  CTA (lb, ms) owns 64 columns l0 = 64*lb of dY and walks
-// its share of the 64-row tiles: dB[:, l0..] += h[m, :]^T * dY[m, l0..]; the
-// ordered cross-CTA reduction is the same as for dA.
+// its share of the 64-row tiles; warp w owns columns l0 + 16w .. +16 and all RP
+// rows of dB:  dB[:, l0..] += h[m, :]^T * dY[m, l0..]  with h from the row
+// pass's hi/lo blob.  Ordered cross-CTA reduction as for dA.
 // =============================================================================
 template <int RP>
-__global__ void __launch_bounds__(NTHREADS) colpass_db_kernel(const __grid_constant__ CUtensorMap tmDY,
-                                                              const __grid_constant__ CUtensorMap tmP,
-                                                              ColArgs p) {
-  using C = ColCfg<RP>;
+struct DbCfg {
+  static constexpr int BLOB = blob_bytes<RP>();
+  static constexpr int STAGE = TILE_BYTES + BLOB;
+  static constexpr int NS = stages_for(STAGE, 2, 8);
+  static constexpr int BYTES = 1024 + NS * STAGE + 8 * (2 * NS) + 16;
+};
+
+template <int RP>
+__global__ void __launch_bounds__(NTHREADS) colpass_db_kernel(const __grid_constant__ CUtensorMap tmDY, ColArgs p) {
+  using C = DbCfg<RP>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  uint8_t *shi = smem + NS * C::STAGE;
-  uint8_t *slo = shi + C::SPLIT;
-  uint64_t *full = reinterpret_cast<uint64_t *>(slo + C::SPLIT + C::SMALL);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * C::STAGE);
   uint64_t *empty = full + NS;
-  int *s_last = reinterpret_cast<int *>(empty + NS + 1);
+  int *s_last = reinterpret_cast<int *>(empty + NS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int lb = blockIdx.x / p.msplit, ms = blockIdx.x % p.msplit;
   const int l0 = lb * BK;
   const int nmt = (p.M + BM - 1) / BM;
   const int t_beg = (int)((int64_t)nmt * ms / p.msplit), t_end = (int)((int64_t)nmt * (ms + 1) / p.msplit);
-  const int cp = p.cp;
-  const uint32_t stage_bytes = TILE_BYTES + cp * 64 * RP * 4;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -667,15 +768,14 @@ __global__ void __launch_bounds__(NTHREADS) colpass_db_kernel(const __grid_const
   if (warp == NCW) {
     if (lane == 0) {
       prefetch_tmap(&tmDY);
-      prefetch_tmap(&tmP);
       int g = 0;
       for (int t = t_beg; t < t_end; ++t, ++g) {
         const int s = g % NS;
         if (g >= NS && !mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) break;
         uint8_t *st = smem + s * C::STAGE;
-        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        mbar_arrive_expect_tx(&full[s], C::STAGE);
         tma_load_2d(st, &tmDY, &full[s], l0, t * BM);
-        tma_load_3d(st + TILE_BYTES, &tmP, &full[s], 0, t * BM, 0);
+        bulk_load(st + TILE_BYTES, p.blob + (size_t)t * C::BLOB, C::BLOB, &full[s]);
       }
     }
     pdl_launch_dependents();
@@ -688,16 +788,12 @@ __global__ void __launch_bounds__(NTHREADS) colpass_db_kernel(const __grid_const
   for (int i = 0; i < RP / 16; ++i)
 #pragma unroll
     for (int n = 0; n < 2; ++n) acc[i][n][0] = acc[i][n][1] = acc[i][n][2] = acc[i][n][3] = 0.f;
-  const uint32_t hb = smem_u32(shi), lbb = smem_u32(slo);
   bool ok = true;
   int g = 0;
   for (int t = t_beg; t < t_end; ++t, ++g) {
     const int s = g % NS;
     if (!(ok = wait_all(&full[s], (g / NS) & 1))) break;
-    uint8_t *st = smem + s * C::STAGE;
-    const uint32_t tb = smem_u32(st);
-    stage_split<RP>(reinterpret_cast<const float *>(st + TILE_BYTES), cp, shi, slo);
-    named_bar_sync(1, NCW * 32);
+    const uint32_t tb = smem_u32(smem + s * C::STAGE), hb = tb + TILE_BYTES, lbb = hb + RP * 128;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       uint32_t b[4];
@@ -713,7 +809,6 @@ __global__ void __launch_bounds__(NTHREADS) colpass_db_kernel(const __grid_const
         mma_bf16(acc[mt][1], al, b[2], b[3]);
       }
     }
-    named_bar_sync(1, NCW * 32);   // split buffers free for the next tile
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
@@ -796,22 +891,14 @@ bool map_bc(CUtensorMap *m, const void *p, int64_t L, int r, int64_t ldb, int RP
   uint32_t box[2] = {(uint32_t)PW, 64};
   return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p, dims, str, box, swz_for(PW * 2));
 }
-// fp32 partials [cp][M][RP]: one box = all cp partials of 64 rows.
-bool map_parts(CUtensorMap *m, const void *p, int64_t M, int RP, int cp) {
-  uint64_t dims[3] = {(uint64_t)RP, (uint64_t)M, (uint64_t)cp};
-  uint64_t str[2] = {(uint64_t)RP * 4, (uint64_t)M * RP * 4};
-  uint32_t box[3] = {(uint32_t)RP, 64, (uint32_t)cp};
-  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
 int pick_pow2(int64_t units, int64_t capacity, int maxv) {
   int c = 1;
   while (c * 2 <= maxv && units * c * 2 <= capacity) c *= 2;
   return c;
 }
 
-int cp_max(int RP) { return RP == 16 ? 4 : RP == 32 ? 2 : 1; }
-constexpr int kMsplitMax = 16;
+constexpr int kCpMax = 4;        // row-pass cluster size (contraction split)
+constexpr int kMsplitMax = 16;   // column-pass split of M
 
 }  // namespace
 
@@ -829,16 +916,15 @@ size_t bf16_ws_bytes(int op, int64_t M, int64_t K, int64_t L, int r) {
   const int RP = rank_bucket(r);
   const size_t packA = ws_round((size_t)r * round_up(K, 8) * 2);
   const size_t packB = ws_round((size_t)L * round_up(r, 8) * 2);
+  const size_t blob = ws_round((size_t)ceil_div(M, BM) * RP * 256);   // hi/lo bf16 of dyb or h
   if (op == LORA_OP_FORWARD) return packA + packB;
   if (op == LORA_OP_BACKWARD_DX_DA) {
     const int64_t nkb = ceil_div(K, 64);
-    return packA + packB + ws_round((size_t)cp_max(RP) * M * RP * 4) +
-           ws_round((size_t)kMsplitMax * nkb * 64 * RP * 4) + ws_round((size_t)nkb * 4);
+    return packA + packB + blob + ws_round((size_t)kMsplitMax * nkb * 64 * RP * 4) + ws_round((size_t)nkb * 4);
   }
   if (op == LORA_OP_BACKWARD_DB) {
     const int64_t nlb = ceil_div(L, 64);
-    return packA + ws_round((size_t)cp_max(RP) * M * RP * 4) + ws_round((size_t)kMsplitMax * RP * nlb * 64 * 4) +
-           ws_round((size_t)nlb * 4);
+    return packA + blob + ws_round((size_t)kMsplitMax * RP * nlb * 64 * 4) + ws_round((size_t)nlb * 4);
   }
   return 0;
 }
@@ -888,13 +974,13 @@ static lora_status_t forward_rp(const SingleArgs &a, void *ws, size_t ws_bytes, 
   auto kern = fwd_bf16_kernel<RP>;
   const size_t smem = FwdCfg<RP>::BYTES;
   LORA_CUDA(ensure_smem((const void *)kern, smem));
-  const int occ = occupancy((const void *)kern, NTHREADS, smem);
+  const int occ = occupancy((const void *)kern, NTHREADS_LS, smem);
   const int64_t nrb = ceil_div(a.M, BM);
   const int64_t nk = ceil_div(a.K, BK), nl = ceil_div(a.L, BK);
   int cl = pick_pow2(nrb, (int64_t)occ * num_sms(), 8);
   while (cl > 1 && (nk < cl || nl < cl)) cl /= 2;
   FwdArgs p{(int)a.M, (int)a.K, (int)a.L, a.scale, cl};
-  LORA_CUDA(launch(kern, dim3((unsigned)(nrb * cl)), dim3(NTHREADS), smem, st, cl, true, tX, tA, tB, tY, p));
+  LORA_CUDA(launch(kern, dim3((unsigned)(nrb * cl)), dim3(NTHREADS_LS), smem, st, cl, true, tX, tA, tB, tY, p));
   return LORA_OK;
 }
 
@@ -907,31 +993,26 @@ lora_status_t forward_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaS
   }
 }
 
-// Row-product partials for dyb (kW_KN) or h.
+// Row pass for dyb (kW_KN) or h: writes the hi/lo blob.
 template <int RP, bool kW_KN>
 static lora_status_t launch_rows(const void *in, int64_t ld_in, int64_t Kc, const CUtensorMap &tW, int64_t M,
-                                 int cp, float *part, int *counters, int ncounters, cudaStream_t st) {
+                                 uint8_t *blob, int *counters, int ncounters, cudaStream_t st) {
   CUtensorMap tIn;
   if (!map_big(&tIn, in, M, Kc, ld_in)) return LORA_ERR_ALIGNMENT;
   auto kern = rows_bf16_kernel<RP, kW_KN>;
   const size_t smem = RowsCfg<RP>::BYTES;
   LORA_CUDA(ensure_smem((const void *)kern, smem));
-  RowsArgs p{(int)M, (int)Kc, cp, part, counters, ncounters};
-  LORA_CUDA(launch(kern, dim3((unsigned)(ceil_div(M, BM) * cp)), dim3(NTHREADS), smem, st, 1, true, tIn, tW, p));
+  const int occ = occupancy((const void *)kern, NTHREADS, smem);
+  const int64_t nrb = ceil_div(M, BM);
+  int cp = pick_pow2(nrb, (int64_t)occ * num_sms(), kCpMax);
+  while (cp > 1 && ceil_div(Kc, BK) < cp) cp /= 2;
+  RowsArgs p{(int)M, (int)Kc, cp, blob, counters, ncounters};
+  LORA_CUDA(launch(kern, dim3((unsigned)(nrb * cp)), dim3(NTHREADS), smem, st, cp, true, tIn, tW, p));
   return LORA_OK;
 }
 
-template <int RP>
-static int choose_cp(int64_t M, int64_t Kc, const void *kern, size_t smem) {
-  const int occ = occupancy(kern, NTHREADS, smem);
-  int cp = pick_pow2(ceil_div(M, BM), (int64_t)occ * num_sms(), cp_max(RP));
-  while (cp > 1 && ceil_div(Kc, BK) < cp) cp /= 2;
-  return cp;
-}
-
-template <int RP>
-static int choose_msplit(int64_t ncol_blocks, int64_t M, const void *kern, size_t smem) {
-  const int occ = occupancy(kern, NTHREADS, smem);
+static int choose_msplit(int64_t ncol_blocks, int64_t M, const void *kern, int threads, size_t smem) {
+  const int occ = occupancy(kern, threads, smem);
   const int64_t cap = (int64_t)occ * num_sms();
   int64_t ms = cap / std::max<int64_t>(ncol_blocks, 1);
   ms = std::min<int64_t>(ms, kMsplitMax);
@@ -949,26 +1030,22 @@ static lora_status_t dxda_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cud
   CUtensorMap tA, tB;
   if (!map_ac(&tA, Ac, a.K, a.r, lay.lda, RP) || !map_bc(&tB, Bc, a.L, a.r, lay.ldb, RP))
     return LORA_ERR_ALIGNMENT;
-  const int cp = choose_cp<RP>(a.M, a.L, (const void *)rows_bf16_kernel<RP, true>, RowsCfg<RP>::BYTES);
-  float *dyb = (float *)carver.take((size_t)cp_max(RP) * a.M * RP * 4);
+  uint8_t *blob = (uint8_t *)carver.take((size_t)ceil_div(a.M, BM) * RP * 256);
   float *partA = (float *)carver.take((size_t)kMsplitMax * nkb * 64 * RP * 4);
   int *counters = (int *)carver.take((size_t)nkb * 4);
-  if (!dyb || !partA || !counters) return LORA_ERR_WORKSPACE;
-  LORA_TRY((launch_rows<RP, true>(a.dY, a.lddy, a.L, tB, a.M, cp, dyb, counters, (int)nkb, st)));
+  if (!blob || !partA || !counters) return LORA_ERR_WORKSPACE;
+  LORA_TRY((launch_rows<RP, true>(a.dY, a.lddy, a.L, tB, a.M, blob, counters, (int)nkb, st)));
 
   auto kern = colpass_dxda_kernel<RP>;
   const size_t smem = ColCfg<RP>::BYTES;
   LORA_CUDA(ensure_smem((const void *)kern, smem));
-  const int ms = choose_msplit<RP>(nkb, a.M, (const void *)kern, smem);
-  CUtensorMap tX, tDX, tP;
-  if (!map_big(&tX, a.X, a.M, a.K, a.ldx) || !map_big(&tDX, a.dX, a.M, a.K, a.lddx) ||
-      !map_parts(&tP, dyb, a.M, RP, cp))
-    return LORA_ERR_ALIGNMENT;
+  const int ms = choose_msplit(nkb, a.M, (const void *)kern, NTHREADS_LS, smem);
+  CUtensorMap tX, tDX;
+  if (!map_big(&tX, a.X, a.M, a.K, a.ldx) || !map_big(&tDX, a.dX, a.M, a.K, a.lddx)) return LORA_ERR_ALIGNMENT;
   ColArgs p{};
   p.M = (int)a.M;
   p.K = (int)a.K;
   p.r = a.r;
-  p.cp = cp;
   p.msplit = ms;
   p.nkb = (int)nkb;
   p.scale = a.scale;
@@ -977,7 +1054,8 @@ static lora_status_t dxda_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cud
   p.out = a.dA;
   p.out_s0 = a.sdA_k;
   p.out_s1 = a.sdA_r;
-  LORA_CUDA(launch(kern, dim3((unsigned)(nkb * ms)), dim3(NTHREADS), smem, st, 1, true, tX, tA, tDX, tP, p));
+  p.blob = blob;
+  LORA_CUDA(launch(kern, dim3((unsigned)(nkb * ms)), dim3(NTHREADS_LS), smem, st, 1, true, tX, tA, tDX, p));
   return LORA_OK;
 }
 
@@ -999,24 +1077,22 @@ static lora_status_t db_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cudaS
   const int64_t nlb = ceil_div(a.L, BK);
   CUtensorMap tA;
   if (!map_ac(&tA, Ac, a.K, a.r, lay.lda, RP)) return LORA_ERR_ALIGNMENT;
-  const int cp = choose_cp<RP>(a.M, a.K, (const void *)rows_bf16_kernel<RP, false>, RowsCfg<RP>::BYTES);
-  float *hpart = (float *)carver.take((size_t)cp_max(RP) * a.M * RP * 4);
+  uint8_t *blob = (uint8_t *)carver.take((size_t)ceil_div(a.M, BM) * RP * 256);
   float *partB = (float *)carver.take((size_t)kMsplitMax * RP * nlb * 64 * 4);
   int *counters = (int *)carver.take((size_t)nlb * 4);
-  if (!hpart || !partB || !counters) return LORA_ERR_WORKSPACE;
-  LORA_TRY((launch_rows<RP, false>(a.X, a.ldx, a.K, tA, a.M, cp, hpart, counters, (int)nlb, st)));
+  if (!blob || !partB || !counters) return LORA_ERR_WORKSPACE;
+  LORA_TRY((launch_rows<RP, false>(a.X, a.ldx, a.K, tA, a.M, blob, counters, (int)nlb, st)));
 
   auto kern = colpass_db_kernel<RP>;
-  const size_t smem = ColCfg<RP>::BYTES;
+  const size_t smem = DbCfg<RP>::BYTES;
   LORA_CUDA(ensure_smem((const void *)kern, smem));
-  const int ms = choose_msplit<RP>(nlb, a.M, (const void *)kern, smem);
-  CUtensorMap tDY, tP;
-  if (!map_big(&tDY, a.dY, a.M, a.L, a.lddy) || !map_parts(&tP, hpart, a.M, RP, cp)) return LORA_ERR_ALIGNMENT;
+  const int ms = choose_msplit(nlb, a.M, (const void *)kern, NTHREADS, smem);
+  CUtensorMap tDY;
+  if (!map_big(&tDY, a.dY, a.M, a.L, a.lddy)) return LORA_ERR_ALIGNMENT;
   ColArgs p{};
   p.M = (int)a.M;
   p.K = (int)a.L;
   p.r = a.r;
-  p.cp = cp;
   p.msplit = ms;
   p.nkb = (int)nlb;
   p.scale = a.scale;
@@ -1025,7 +1101,8 @@ static lora_status_t db_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cudaS
   p.out = a.dB;
   p.out_s0 = a.sdB_r;
   p.out_s1 = a.sdB_l;
-  LORA_CUDA(launch(kern, dim3((unsigned)(nlb * ms)), dim3(NTHREADS), smem, st, 1, true, tDY, tP, p));
+  p.blob = blob;
+  LORA_CUDA(launch(kern, dim3((unsigned)(nlb * ms)), dim3(NTHREADS), smem, st, 1, true, tDY, p));
   return LORA_OK;
 }
 

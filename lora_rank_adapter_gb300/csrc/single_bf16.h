@@ -40,18 +40,19 @@ struct FwdArgs {
 
 struct RowsArgs {
   int M, Kc, csplit;
-  float *part;
+  uint8_t *blob;     // [ceil(M/64)] x (hi, lo) bf16 [64][RP] tiles
   int *counters;
   int ncounters;
 };
 
 struct ColArgs {
-  int M, K, r, cp, msplit, nkb;   // for dB, K holds L and nkb the number of 64-column blocks of L
+  int M, K, r, msplit, nkb;   // for dB, K holds L and nkb the number of 64-column blocks of L
   float scale;
   float *part_out;
   int *counters;
   float *out;
   int64_t out_s0, out_s1;
+  const uint8_t *blob;        // the row pass's hi/lo tiles of dyb (dX/dA) or h (dB)
 };
 
 SingleLayout plan_layout(const SingleArgs &a, bool need_A, bool need_B);

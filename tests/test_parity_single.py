@@ -119,6 +119,17 @@ def test_single_bf16_small(M, K, L, r, mode):
     check_all(w, spec["s"], out, TOL_BF16)
 
 
+@pytest.mark.parametrize("M,K,L,r", [(8192, 64, 64, 128), (6000, 128, 72, 64), (5000, 64, 200, 16),
+                                     (4096, 136, 64, 100)])
+def test_single_bf16_many_tiles_per_cta(M, K, L, r):
+    """Narrow K / L and tall M: each column-pass CTA walks many more row tiles than
+    it has pipeline stages, so every stage is reused several times."""
+    spec = synth.single_spec("single_c2", M=M, K=K, L=L, r=r)
+    w = synth.make_single(spec, seed=M + r, device=DEV)
+    out = run_all(w, spec["s"], "peft")
+    check_all(w, spec["s"], out, TOL_BF16)
+
+
 @pytest.mark.parametrize("M,K,L,r", [(3, 24, 40, 3), (130, 200, 72, 16), (65, 96, 128, 33)])
 def test_single_bf16_strided_small_operands(M, K, L, r):
     spec = synth.single_spec("single_c2", M=M, K=K, L=L, r=r)
