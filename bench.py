@@ -22,6 +22,8 @@ import argparse
 import hashlib
 import json
 import math
+
+import numpy as np
 import os
 import statistics
 import subprocess
@@ -151,6 +153,40 @@ def single_bytes(M, K, L, r):
     }
 
 
+MULTI_SPEC = dict(T=8192, IN=4096)   # the q_proj batch as a fused-QKV serving target
+
+
+def build_multi(torch, synth, dev, k, X):
+    spec = synth.multi_spec("multi_c4", **MULTI_SPEC)
+    w = synth.make_multi(spec, seed=SEED + k, device=dev)
+    w["x"] = X                                    # the same batch of tokens
+    w["y"] = w["y0"].clone()
+    w["h"] = torch.zeros((spec["T"], len(spec["out_slices"]) * spec["R"]), dtype=torch.float32, device=dev)
+    w["spec"] = spec
+    return w
+
+
+def multi_bytes(w):
+    """Algorithmic bytes: active tokens only, rank-limited columns, each used
+    slot's adapter weights once."""
+    slots = w["slots"].cpu().tolist()
+    ranks = w["ranks"].cpu().tolist()
+    S, R, IN = w["S"], w["R"], w["IN"]
+    osl = w["out_slices"]
+    n, O = len(osl), sum(osl)
+    act = [t for t, s in enumerate(slots) if 0 <= s < S and 1 <= ranks[s] <= R]
+    used = sorted({slots[t] for t in act})
+    na = len(act)
+    hcols = sum(n * ranks[slots[t]] for t in act)          # specified h entries
+    a_b = sum(n * ranks[s] * IN * 2 for s in used)
+    b_b = sum(ranks[s] * O * 2 for s in used)
+    return {
+        "lora_shrink": na * IN * 2 + a_b + hcols * 4,
+        "lora_expand": hcols * 4 + 2 * na * O * 2 + b_b,
+        "lora_apply_linear": na * IN * 2 + a_b + b_b + 2 * na * O * 2,
+    }
+
+
 def make_ops(torch, lora, binding, synth, dev):
     """Per input set: the list of (name, callable, bytes) that makes one step."""
     sets = []
@@ -160,8 +196,22 @@ def make_ops(torch, lora, binding, synth, dev):
         r, L = w["B"].shape
         ws = {op: binding.workspace(op, binding.LORA_BF16, M, K, L, r, device=dev)
               for op in (binding.OP_FORWARD, binding.OP_BACKWARD_DX_DA, binding.OP_BACKWARD_DB)}
-        sets.append(dict(w=w, ws=ws, M=M, K=K, L=L, r=r))
+        mw = build_multi(torch, synth, dev, k, w["X"])
+        O = sum(mw["out_slices"])
+        for op in (binding.OP_SHRINK, binding.OP_EXPAND, binding.OP_APPLY_LINEAR):
+            ws[op] = binding.workspace(op, binding.LORA_BF16, mw["T"], mw["IN"], O, mw["R"], mw["S"], device=dev)
+        sets.append(dict(w=w, mw=mw, ws=ws, M=M, K=K, L=L, r=r))
+    # embedding target: ids of the batch over a 128256-entry axis (one shared table)
+    gspec = synth.multi_spec("multi_c5", T=sets[0]["M"], IN=64, out_slices=[64], S=32)
+    gw = synth.make_multi(gspec, seed=SEED, device=dev)
+    gw["hg"] = torch.zeros((gspec["T"], gspec["R"]), dtype=torch.float32, device=dev)
     by = single_bytes(sets[0]["M"], sets[0]["K"], sets[0]["L"], sets[0]["r"])
+    by.update(multi_bytes(sets[0]["mw"]))
+    ga = gw["ga"]
+    gslots, granks, gids = gw["slots"], gw["ranks"], gw["ids"]
+    act = [(s, i) for s, i in zip(gslots.cpu().tolist(), gids.cpu().tolist())]
+    rk = granks.cpu().tolist()
+    by["lora_gather_shrink"] = sum(rk[s] * (2 + 4) for s, i in act if 0 <= i < ga.shape[2]) + 8 * len(act)
 
     def fwd(S):
         w = S["w"]
@@ -176,32 +226,68 @@ def make_ops(torch, lora, binding, synth, dev):
         w = S["w"]
         lora.lora_backward_db(w["X"], w["A"], w["dY"], w["s"], w["dB"], ws=S["ws"][binding.OP_BACKWARD_DB])
 
+    def shrink(S):
+        m = S["mw"]
+        lora.lora_shrink(m["x"], m["a"], m["slots"], m["ranks"], m["R"], m["h"], num_slices=len(m["out_slices"]),
+                         ws=S["ws"][binding.OP_SHRINK])
+
+    def expand(S):
+        m = S["mw"]
+        lora.lora_expand(m["h"], m["b"], m["slots"], m["ranks"], m["scalings"], m["y"], m["out_slices"], m["R"],
+                         ws=S["ws"][binding.OP_EXPAND])
+
+    def apply(S):
+        m = S["mw"]
+        lora.lora_apply_linear(m["x"], m["a"], m["b"], m["slots"], m["ranks"], m["scalings"], m["y"],
+                               m["out_slices"], m["R"], ws=S["ws"][binding.OP_APPLY_LINEAR])
+
+    def gather(S):
+        lora.lora_gather_shrink(gids, ga, gslots, granks, gw["R"], gw["hg"])
+
     ops = [("lora_forward", fwd, by["lora_forward"]),
            ("lora_backward_dx_da", dxda, by["lora_backward_dx_da"]),
-           ("lora_backward_db", db, by["lora_backward_db"])]
+           ("lora_backward_db", db, by["lora_backward_db"]),
+           ("lora_shrink", shrink, by["lora_shrink"]),
+           ("lora_expand", expand, by["lora_expand"]),
+           ("lora_apply_linear", apply, by["lora_apply_linear"]),
+           ("lora_gather_shrink", gather, by["lora_gather_shrink"])]
     return sets, ops, sets[0]["M"]
 
 
 def h2d_d2h_tensors(S):
     """(inputs copied in, results copied out) of one step, for the end-to-end leg."""
-    w = S["w"]
-    ins = [w["X"], w["Y"], w["dY"]]
-    outs = [w["Y"], w["dX"], w["dA"], w["dB"]]
+    w, m = S["w"], S["mw"]
+    ins = [w["X"], w["Y"], w["dY"], m["y"]]
+    outs = [w["Y"], w["dX"], w["dA"], w["dB"], m["h"], m["y"]]
     return ins, outs
 
 
 # ----------------------------------------------------------------------------- oracle timing
 def oracle_sample_pass(O, synth, torch, tokens):
-    """One pass of the oracle over a `tokens`-row sample of the workload."""
+    """One pass of the oracle over a `tokens`-row sample of the workload (every
+    op of the step; the gather over a 4096-entry axis, its cost per token does
+    not depend on the axis length)."""
     spec = synth.single_spec("single_c2", M=tokens)
     gen = "cuda" if torch.cuda.is_available() else "cpu"
     w = synth.make_single(spec, seed=SEED, device=gen, prefix="cpu")
     f = lambda t: t.double().cpu().numpy()
     X, A, B, Y0, dY = (f(w[k]) for k in ("X", "A", "B", "Y0", "dY"))
+    ms = synth.multi_spec("multi_c4", T=tokens, IN=4096)
+    mw = synth.make_multi(ms, seed=SEED, device=gen)
+    gs = synth.multi_spec("multi_c5", T=tokens, IN=64, out_slices=[64], S=32, V=4096)
+    gw = synth.make_multi(gs, seed=SEED, device=gen)
+    sl, rk, sc = (mw[k].cpu().numpy() for k in ("slots", "ranks", "scalings"))
+    a, b, y0 = f(mw["a"]), f(mw["b"]), f(mw["y0"])
+    ga, gsl, grk, gid = f(gw["ga"]), gw["slots"].cpu().numpy(), gw["ranks"].cpu().numpy(), gw["ids"].cpu().numpy()
+    R, osl = ms["R"], ms["out_slices"]
     t0 = time.perf_counter()
     O.forward(X, A, B, Y0, spec["s"])
     O.backward_dx_da(X, dY, A, B, spec["s"])
     O.backward_db(X, A, dY, spec["s"])
+    h = O.shrink(X, a, sl, rk, R, len(osl))
+    O.expand(h, b, sl, rk, sc.astype(np.float64), y0, osl, R)
+    O.apply_linear(X, a, b, sl, rk, sc.astype(np.float64), y0, osl, R)
+    O.gather_shrink(gid, ga, gsl, grk, gs["R"])
     return time.perf_counter() - t0
 
 
@@ -216,7 +302,7 @@ def cpu_baseline(torch, synth, target_s=12.0):
         tokens = min(2048, tokens * 4)
         dt = oracle_sample_pass(O, synth, torch, tokens)
     return {"value": tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{tokens} of the 8192 tokens through fwd + dX/dA + dB (fp64, one pass, {dt:.2f} s)"}
+            "sample": f"{tokens} of the 8192 tokens through every op of the step (fp64, one pass, {dt:.2f} s)"}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -240,7 +326,7 @@ def run_reference(args, rank, world):
             "data": "synthetic (seeded SplitMix64)",
             "config": {"workload": WORKLOAD, "global_batch": 8192, "seq_len": 2048, "parallelism": "replicas"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{tokens} of the 8192 tokens per step through fwd + dX/dA + dB (fp64)"},
+                             "sample": f"{tokens} of the 8192 tokens per step through every op of the step (fp64)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
