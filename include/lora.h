@@ -157,6 +157,32 @@ LORA_API lora_status_t lora_backward_db(lora_dtype_t dtype, int64_t M, int64_t K
                                void *ws, size_t ws_bytes, void *stream);
 
 /* --------------------------------------------------------------------------------
+ * lora_backward_db_noalloc: lora_backward_db for callers that cannot allocate
+ * device memory.  The pages have no counterpart of this entry point; it exists
+ * for code that runs where the surrounding system owns all device memory (an
+ * operator inside another engine's memory pool, a plugin that is handed tensors
+ * but no allocator) or where a cudaMalloc, with its implicit device-wide
+ * synchronisation, cannot be afforded on the hot path.
+ *   Arguments, results and errors are those of lora_backward_db, without ws /
+ *   ws_bytes.  Scratch comes from a LORA_DB_NOALLOC_SCRATCH_BYTES array of the
+ *   library's own device memory, which every GPU that loads the library holds
+ *   until the process exits.  Sizes whose lora_workspace_size(LORA_OP_BACKWARD_DB,
+ *   ...) exceeds it are rejected with LORA_ERR_WORKSPACE before anything is
+ *   launched.  No cudaMalloc, cudaFree or allocating library call is made.
+ *   The first call on a device looks up the array's device address on that
+ *   device (the device current at the call); make that first call before any
+ *   stream capture.  All calls share the one array and the kernels re-clear what
+ *   must start at zero on every call, but two calls that can run at the same time
+ *   on the GPU (other streams, other host threads) race on it: serialise them.
+ * -------------------------------------------------------------------------------- */
+#define LORA_DB_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+LORA_API lora_status_t lora_backward_db_noalloc(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r,
+                               const void *X, int64_t ldx,
+                               const void *A, int64_t sA_k, int64_t sA_r,
+                               const void *dY, int64_t lddy, float scale,
+                               float *dB, int64_t sdB_r, int64_t sdB_l, void *stream);
+
+/* --------------------------------------------------------------------------------
  * lora_group_by_slot: the integer step in front of the segmented kernels.
  * counts[s] = number of active tokens on slot s; perm[0..n) = the active tokens
  * ordered by (slot, token index) (a stable counting sort); *num_active = n.

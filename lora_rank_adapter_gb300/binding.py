@@ -23,7 +23,7 @@ STATUS = {0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_UNSUPPORTED", 3:
 EXPORTS = ["lora_workspace_size", "lora_forward", "lora_backward_dx_da", "lora_backward_db",
            "lora_group_by_slot", "lora_shrink", "lora_expand", "lora_apply_linear",
            "lora_gather_shrink", "lora_status_string", "lora_device_error", "lora_kernel_launches",
-           "lora_version"]
+           "lora_version", "lora_backward_db_noalloc"]
 
 
 class LoraError(RuntimeError):
@@ -69,6 +69,8 @@ def lib():
         "lora_status_string": (ctypes.c_char_p, [i32]),
         "lora_device_error": (i32, [ctypes.POINTER(i32)]),
         "lora_kernel_launches": (ctypes.c_uint64, []),
+        "lora_backward_db_noalloc": (i32, [i32, i64, i64, i64, i32, P, i64, P, i64, i64, P, i64, f32, P, i64, i64,
+                                           P]),
         "lora_version": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
