@@ -3,21 +3,25 @@
 // Operations (mstar page "mstar.engine.resources.lora.ops"):
 //   shrink         h[t, i*R + j] = x[t] . a[slot(t)][i*R + j]            (j < rank)
 //   expand_fused   y[t, slice i] += scalings[slot] * h[t, slice i] @ b[slot, slice i]^T
-//   apply_linear_  shrink then expand (fused here; h never leaves the chip)
+//   apply_linear_  shrink then expand into y
 //   gather_shrink  h[t] = a[slot(t)][:, ids[t]]  (ids outside [0, V) give zeros)
 // and the integer step in front of them (group_by_slot): a stable counting sort
 // of the active tokens by slot and a list of tiles of at most 64 tokens of one
 // slot, built on the device with no host sync (the page requires the ops to run
 // without one).
 //
-// The segmented kernel runs one token tile per cluster of `cl` CTAs.  Phase 1
-// (shrink) splits the contraction over the cluster and sums the partial h in
-// cluster-rank order through distributed shared memory; phase 2 (expand) splits
-// the output column blocks over the cluster.  Rows are gathered (the tile's
-// tokens need not be contiguous) with one 1-D bulk copy per row into padded
-// shared-memory rows (144-byte pitch, conflict-free ldmatrix); y rows go back
-// the same way from a storer warp.  Adapter padding (rows / columns past a
-// slot's rank, which may hold anything) is masked in registers, never trusted.
+// shrink_kernel: one (token tile, slice) per cluster of `cl` CTAs; the
+// contraction is split over the cluster and the partial h are summed in
+// cluster-rank order through distributed shared memory.
+// expand_kernel: one (token tile, slice, group of 64-column blocks) per CTA;
+// only that slice's h is held in registers, y blocks stream through a ring with
+// a loader and a storer warp.
+// apply_linear runs both, chained by programmatic dependent launch, with h in
+// the workspace (it stays in L2 between the two kernels).
+// Rows are gathered (a tile's tokens need not be contiguous) with one 1-D bulk
+// copy per row into padded shared-memory rows (conflict-free ldmatrix).
+// Adapter padding (rows / columns past a slot's rank, which may hold anything)
+// is masked in registers, never trusted.
 #include <algorithm>
 
 #include "common.cuh"
@@ -28,33 +32,44 @@ namespace lora {
 
 namespace {
 
-constexpr int MBM = 64;                   // token rows per tile
-constexpr int MCW = 4;                    // consumer warps
-constexpr int MTHREADS = (MCW + 2) * 32;  // + loader + storer
-constexpr int KW = 64;                    // contraction columns per phase-1 stage
-constexpr int XP = KW * 2 + 16;           // padded row pitch (bytes) of x / a / y rows
-constexpr int CBW = 64;                   // output columns per phase-2 block
-constexpr int kMaxHC = 256;               // n * R columns of h held on chip
+constexpr int MBM = 64;      // token rows per tile
+constexpr int KW = 64;       // contraction columns per shrink stage
+constexpr int XP = KW * 2 + 16;   // padded row pitch (bytes) of x / a / y rows in shared memory
+constexpr int CBW = 64;      // output columns per expand block
+constexpr int kMaxHC = 256;  // n * R columns of h held on chip by the shrink
 
-enum Mode { kShrink = 0, kExpand = 1, kApply = 2 };
+constexpr int EX_CW = 4;     // expand consumer warps (16 rows each)
 
-struct SegArgs {
-  const int32_t *slots, *ranks;
+struct MArgs {
+  const int32_t *ranks;
   const float *scal;
   const int *header;   // [0] number of active tokens, [1] number of tiles
   const int4 *tiles;   // (slot, start, len, 0)
   const int32_t *perm;
-  int T, S, R, n, cl;
+  int S, R, n, cl, gb, ngroups;
   int64_t in;
   const __nv_bfloat16 *x; int64_t ldx;
   const __nv_bfloat16 *a; int64_t sa_slot, sa_row;
   const __nv_bfloat16 *b; int64_t sb_slot, sb_row;
   float *h; int64_t ldh;
   __nv_bfloat16 *y; int64_t ldy;
-  int nb;                      // number of (slice, column block) pairs
-  int off[LORA_MAX_SLICES + 1];
-  int blk0[LORA_MAX_SLICES + 1];   // first block index of each slice
+  int off[LORA_MAX_SLICES + 1];   // output column offset of each slice
+  int tma_ok;                     // the tensor maps of x / y are valid
 };
+
+// Byte offset of (row, col) in a 64 x 64 bf16 tile written by TMA with the
+// 128-byte swizzle (tile base 1024-byte aligned).
+__device__ __forceinline__ uint32_t swz_off(int row, int col) { return swz(row, col * 2, 128); }
+
+// A tile is "dense" when its 64 tokens are consecutive rows: then x / y tiles
+// can move as one TMA box instead of 64 gathered rows (LORA_MULTI_TMA selects
+// which kernels use that path: bit 0 the shrink, bit 1 the expand).
+#ifndef LORA_MULTI_TMA
+#define LORA_MULTI_TMA 1
+#endif
+__device__ __forceinline__ bool dense_tile(const int32_t *perm, int start, int len) {
+  return len == 64 && perm[start + 63] - perm[start] == 63;
+}
 
 __device__ __forceinline__ uint32_t mask_pair(uint32_t v, int j0, int lim) {
   // keep the bf16 halves whose column j0 (low) / j0 + 1 (high) is below lim
@@ -63,24 +78,13 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t v, int j0, int lim) {
 }
 
 template <int N>
-__device__ __forceinline__ void bulk_wait_read_n() {
+__device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
-
-template <int HC>
-struct SegCfg {
-  static constexpr int P1 = (MBM + HC) * XP;              // x rows + a rows
-  static constexpr int BP = 2 * 128 + 16;                 // max b-row pitch (R <= 128)
-  static constexpr int P2 = MBM * XP + CBW * BP;          // y rows + b rows
-  static constexpr int STAGE = ((P1 > P2 ? P1 : P2) + 1023) / 1024 * 1024;
-  static constexpr int NS = (72 * 1024) / STAGE < 2 ? 2 : (72 * 1024) / STAGE > 6 ? 6 : (72 * 1024) / STAGE;
-  static constexpr int BYTES = 1024 + NS * STAGE + 8 * (3 * NS + 4) + 64;
-  static_assert(MBM * HC * 4 <= NS * STAGE, "h exchange must fit in the stage ring");
-};
 
 // Warp-uniform bounded wait.
 template <bool kCluster = false>
@@ -99,6 +103,10 @@ __device__ __forceinline__ void ldb_p(uint32_t base, int pitch, int n0, int k0, 
           b[3]);
 }
 
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+  return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
 }  // namespace
 
 // =============================================================================
@@ -107,7 +115,8 @@ __device__ __forceinline__ void ldb_p(uint32_t base, int pitch, int n0, int k0, 
 // atomics), a block scan turns the counts into per-(warp, slot) cursors, and
 // pass 2 revisits the ranges in the same order and scatters each token to its
 // cursor: a stable counting sort by slot.  Tiles of at most `bmt` tokens of one
-// slot are then listed in slot order.
+// slot are listed in slot order.  Slots are read in batches of 8 per lane so
+// their loads overlap.
 // =============================================================================
 __device__ __forceinline__ void block_scan2(int a, int b, int &ea, int &eb, int &ta, int &tb, int *sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -153,6 +162,8 @@ __device__ __forceinline__ void block_scan2(int a, int b, int &ea, int &eb, int 
   __syncthreads();
 }
 
+constexpr int GU = 8;   // tokens per lane per batch in group_kernel
+
 __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__ slots, int T, int S, int R,
                                                      const int32_t *__restrict__ ranks, int32_t *counts_out,
                                                      int32_t *perm_out, int32_t *num_active_out, int *header,
@@ -160,20 +171,38 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
   extern __shared__ int gsm[];
   const int nw = blockDim.x >> 5;
   int *hist = gsm;                 // [nw][S]
-  int *sh = gsm + nw * S;          // scan scratch (160 ints)
+  int *srank = gsm + nw * S;       // [S]
+  int *sh = srank + S;             // scan scratch (160 ints)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
-  for (int i = threadIdx.x; i < nw * S; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
   const int t_lo = (int)((int64_t)T * warp / nw), t_hi = (int)((int64_t)T * (warp + 1) / nw);
+  const bool one_batch = t_hi - t_lo <= 32 * GU;   // the warp's slots stay in registers for both passes
+  int sv[GU];
+#pragma unroll
+  for (int u = 0; u < GU; ++u) {
+    const int t = t_lo + u * 32 + lane;
+    sv[u] = t < t_hi ? slots[t] : -1;
+  }
+  for (int i = threadIdx.x; i < nw * S; i += blockDim.x) hist[i] = 0;
+  for (int i = threadIdx.x; i < S; i += blockDim.x) srank[i] = ranks[i];
+  __syncthreads();
   const unsigned lt = (1u << lane) - 1u;
-  for (int t0 = t_lo; t0 < t_hi; t0 += 32) {
-    const int t = t0 + lane;
-    const int s = t < t_hi ? slots[t] : -1;
-    const bool act = t < t_hi && s >= 0 && s < S && ranks[s] >= 1 && ranks[s] <= R;
-    const unsigned m = __match_any_sync(0xffffffffu, act ? s : -(lane + 1));
-    if (act && (m & lt) == 0) hist[warp * S + s] += __popc(m);
-    __syncwarp();
+  auto active = [&](int s) { return s >= 0 && s < S && srank[s] >= 1 && srank[s] <= R; };
+  for (int t0 = t_lo; t0 < t_hi; t0 += 32 * GU) {
+    if (t0 != t_lo) {
+#pragma unroll
+      for (int u = 0; u < GU; ++u) {
+        const int t = t0 + u * 32 + lane;
+        sv[u] = t < t_hi ? slots[t] : -1;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < GU; ++u) {
+      const bool act = active(sv[u]);
+      const unsigned m = __match_any_sync(0xffffffffu, act ? sv[u] : -(lane + 1));
+      if (act && (m & lt) == 0) hist[warp * S + sv[u]] += __popc(m);
+      __syncwarp();
+    }
   }
   __syncthreads();
   int run = 0, trun = 0;
@@ -205,317 +234,468 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
     header[1] = trun;
   }
   __syncthreads();
-  for (int t0 = t_lo; t0 < t_hi; t0 += 32) {
-    const int t = t0 + lane;
-    const int s = t < t_hi ? slots[t] : -1;
-    const bool act = t < t_hi && s >= 0 && s < S && ranks[s] >= 1 && ranks[s] <= R;
-    const unsigned m = __match_any_sync(0xffffffffu, act ? s : -(lane + 1));
-    int cur = 0;
-    if (act) cur = hist[warp * S + s];
-    __syncwarp();
-    if (act) {
-      perm_out[cur + __popc(m & lt)] = t;
-      if ((m & lt) == 0) hist[warp * S + s] = cur + __popc(m);
+  for (int t0 = t_lo; t0 < t_hi; t0 += 32 * GU) {
+    if (!one_batch) {
+#pragma unroll
+      for (int u = 0; u < GU; ++u) {
+        const int t = t0 + u * 32 + lane;
+        sv[u] = t < t_hi ? slots[t] : -1;
+      }
     }
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < GU; ++u) {
+      const int t = t0 + u * 32 + lane;
+      const bool act = active(sv[u]);
+      const unsigned m = __match_any_sync(0xffffffffu, act ? sv[u] : -(lane + 1));
+      int cur = 0;
+      if (act) cur = hist[warp * S + sv[u]];
+      __syncwarp();
+      if (act) {
+        perm_out[cur + __popc(m & lt)] = t;
+        if ((m & lt) == 0) hist[warp * S + sv[u]] = cur + __popc(m);
+      }
+      __syncwarp();
+    }
   }
   pdl_launch_dependents();
 }
 
+// 16-byte asynchronous global -> shared copies (src_bytes < 16 zero-fills the
+// rest), and an mbarrier arrival once all of this thread's earlier copies landed.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ uint32_t clamp16(int v) { return v <= 0 ? 0u : v >= 16 ? 16u : (uint32_t)v; }
+
+constexpr int LDW = 2;                 // loader warps (64 threads) of the multi-adapter kernels
+constexpr int LDT = LDW * 32;
+constexpr int RPT = MBM * 8 / LDT;     // tile rows handled per loader thread (8 sixteen-byte chunks a row)
+
 // =============================================================================
-// The segmented kernel.  MODE kShrink: phase 1 and the h write; kExpand: h read
-// and phase 2; kApply: phase 1 then phase 2 with h in registers.
+// shrink_kernel: CTA (tile, slice i) computes h[t, i*R + j] = x[t] . a[slot][i*R + j]
+// for j < rank.  A cluster of `cl` CTAs splits the contraction (decode tiles are
+// few) and sums the partial h in cluster-rank order through distributed shared
+// memory.  Four consumer warps own 16 rows each; two loader warps gather the
+// tile's x rows (one TMA box when the tile is dense) and the slice's a rows
+// with 16-byte cp.async copies.
 // =============================================================================
-template <int HC, int MODE>
-__global__ void __launch_bounds__(MTHREADS) seg_kernel(SegArgs p) {
-  using C = SegCfg<HC>;
+constexpr int SH_CWN = 4;   // shrink consumer warps
+
+template <int RP>
+struct ShCfg {
+  static constexpr int STAGE = ((MBM + RP) * XP + 1023) / 1024 * 1024;   // x rows + a rows of one slice
+  static constexpr int NS = (54 * 1024) / STAGE < 2 ? 2 : (54 * 1024) / STAGE > 6 ? 6 : (54 * 1024) / STAGE;
+  static constexpr int BYTES = 1024 + NS * STAGE + 8 * (2 * NS + 2) + 64;
+  static constexpr int THREADS = (SH_CWN + LDW) * 32;
+  static_assert(MBM * RP * 4 <= NS * STAGE, "the h exchange must fit in the stage ring");
+};
+
+template <int RP>
+__global__ void __launch_bounds__(ShCfg<RP>::THREADS, RP >= 128 ? 2 : 4)
+    shrink_kernel(const __grid_constant__ CUtensorMap tmX, MArgs p) {
+  using C = ShCfg<RP>;
   constexpr int NS = C::NS;
-  constexpr bool P1 = MODE != kExpand, P2 = MODE != kShrink;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *smem = align1024(smem_raw);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * C::STAGE);
-  uint64_t *done = full + NS;
-  uint64_t *freeb = done + NS;
-  uint64_t *hready = freeb + NS, *hdone = hready + 1, *xready = hready + 2;
-  float *hbuf = reinterpret_cast<float *>(smem);   // the h exchange reuses the stage ring
+  uint64_t *empty = full + NS;
+  uint64_t *hready = empty + NS, *hdone = hready + 1;
+  float *hbuf = reinterpret_cast<float *>(smem);   // the exchange reuses the ring once the loads are over
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cl = p.cl;
-  const int tile = blockIdx.x / cl;
+  const int item = blockIdx.x / cl;
+  const int tile = item / p.n, i = item % p.n;
   pdl_wait();
-  if (tile >= p.header[1]) return;   // whole cluster: beyond the device-side tile count
+  if (tile >= p.header[1]) return;   // the whole cluster: beyond the device-side tile count
   const uint32_t crank = cl > 1 ? cluster_ctarank() : 0u;
   const int4 td = p.tiles[tile];
   const int slot = td.x, start = td.y, len = td.z;
   const int rank = p.ranks[slot];
-  const int R = p.R, n = p.n;
-  const int nk = P1 ? (int)((p.in + KW - 1) / KW) : 0;
+  const bool dense = (LORA_MULTI_TMA & 1) && p.tma_ok && dense_tile(p.perm, start, len);
+  const int nk = (int)((p.in + KW - 1) / KW);
   const int k_beg = (int)((int64_t)nk * crank / cl), k_end = (int)((int64_t)nk * (crank + 1) / cl);
-  const int b_beg = P2 ? (int)((int64_t)p.nb * crank / cl) : 0, b_end = P2 ? (int)((int64_t)p.nb * (crank + 1) / cl) : 0;
-  const int n1 = k_end - k_beg, ntiles = n1 + (b_end - b_beg);
-  const int r16 = (R + 15) & ~15, rank8 = (rank + 7) & ~7;
-  const int bp = r16 * 2 + 16;   // b-row pitch in bytes
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 32);
-      mbar_init(&done[s], MCW);
-      mbar_init(&freeb[s], 1);
+      mbar_init(&full[s], LDT + 1);
+      mbar_init(&empty[s], SH_CWN);
     }
-    mbar_init(hready, cl > 1 ? MCW * 32 * (cl - 1) : 1);
-    mbar_init(hdone, cl > 1 ? MCW * 32 * (cl - 1) : 1);
-    mbar_init(xready, MCW * 32);
+    mbar_init(hready, cl > 1 ? SH_CWN * 32 * (cl - 1) : 1);
+    mbar_init(hdone, cl > 1 ? SH_CWN * 32 * (cl - 1) : 1);
     fence_barrier_init();
   }
   if (cl > 1) cluster_sync_all(); else __syncthreads();
 
-  // (slice, column block) of phase-2 block index q
-  auto blk = [&](int q, int &i, int &c0, int &ocols) {
-    i = 0;
-    while (i + 1 < n && q >= p.blk0[i + 1]) ++i;
-    c0 = p.off[i] + (q - p.blk0[i]) * CBW;
-    ocols = min(CBW, p.off[i + 1] - c0);
-  };
-
-  if (warp == MCW) {
-    // ---------------------------------------------------------------- loader (32 lanes)
-    for (int g = 0; g < ntiles; ++g) {
+  if (warp >= SH_CWN) {
+    // ---------------------------------------------------------------- loaders (64 threads)
+    const int lt = threadIdx.x - SH_CWN * 32;
+    const int ch = lt & 7;                         // 16-byte chunk of a row
+    const int t0 = p.perm[start];
+    if (lt == 0 && dense) prefetch_tmap(&tmX);
+    const __nv_bfloat16 *xrow[RPT];
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) {
+      const int r = (lt >> 3) + k * (LDT / 8);
+      xrow[k] = r < len ? p.x + (int64_t)p.perm[start + r] * p.ldx : p.x;
+    }
+    const __nv_bfloat16 *as = p.a + (int64_t)slot * p.sa_slot + (int64_t)i * p.R * p.sa_row;
+    for (int g = 0; g < k_end - k_beg; ++g) {
       const int s = g % NS;
-      if (g >= NS && !mbar_wait(&freeb[s], ((g / NS) & 1) ^ 1)) break;
-      if (P1 && P2 && cl > 1 && g == n1 && !mbar_wait(xready, 0)) break;   // stage ring holds the exchange
+      if (g >= NS && !mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) break;
       uint8_t *st = smem + s * C::STAGE;
-      uint32_t bytes = 0;
-      if (g < n1) {
-        const int64_t k0 = (int64_t)(k_beg + g) * KW;
-        const int kb = (int)(p.in - k0 < (int64_t)KW ? p.in - k0 : (int64_t)KW);
-        const uint32_t rb = kb * 2;
-        // expect first, then copies, then (after zeroing a ragged tail) arrive
-        int cnt = 0;
-        for (int r = lane; r < len; r += 32) ++cnt;
-        for (int c = lane; c < n * R; c += 32)
-          if (c % R < rank) ++cnt;
-        mbar_expect_tx(&full[s], cnt * rb);
-        for (int r = lane; r < len; r += 32)
-          bulk_load(st + r * XP, p.x + (int64_t)p.perm[start + r] * p.ldx + k0, rb, &full[s]);
-        const __nv_bfloat16 *as = p.a + (int64_t)slot * p.sa_slot + k0;
-        for (int c = lane; c < n * R; c += 32)
-          if (c % R < rank) bulk_load(st + (MBM + c) * XP, as + (int64_t)c * p.sa_row, rb, &full[s]);
-        if (kb < KW) {   // zero the tail columns of every loaded row (they enter the contraction)
-          for (int r = lane; r < len; r += 32)
-            for (int cc = rb; cc < KW * 2; cc += 16) *reinterpret_cast<int4 *>(st + r * XP + cc) = make_int4(0, 0, 0, 0);
-          for (int c = lane; c < n * R; c += 32)
-            if (c % R < rank)
-              for (int cc = rb; cc < KW * 2; cc += 16)
-                *reinterpret_cast<int4 *>(st + (MBM + c) * XP + cc) = make_int4(0, 0, 0, 0);
+      const int64_t k0 = (int64_t)(k_beg + g) * KW;
+      const int64_t krem = p.in - k0 < (int64_t)KW ? p.in - k0 : (int64_t)KW;
+      const uint32_t nb = clamp16((int)krem * 2 - ch * 16);
+      if (dense) {
+        if (lt == 0) {
+          mbar_arrive_expect_tx(&full[s], MBM * KW * 2);
+          tma_load_2d(st, &tmX, &full[s], (int)k0, t0);
         }
-        (void)bytes;
       } else {
-        int i, c0, ocols;
-        blk(b_beg + g - n1, i, c0, ocols);
-        const uint32_t yb = ocols * 2, bb = rank8 * 2;
-        int cnt = 0;
-        for (int r = lane; r < len; r += 32) ++cnt;
-        int cb = 0;
-        for (int cc = lane; cc < ocols; cc += 32) ++cb;
-        mbar_expect_tx(&full[s], cnt * yb + cb * bb);
-        for (int r = lane; r < len; r += 32)
-          bulk_load(st + r * XP, p.y + (int64_t)p.perm[start + r] * p.ldy + c0, yb, &full[s]);
-        const __nv_bfloat16 *bs = p.b + (int64_t)slot * p.sb_slot;
-        for (int cc = lane; cc < ocols; cc += 32)
-          bulk_load(st + MBM * XP + cc * bp, bs + (int64_t)(c0 + cc) * p.sb_row, bb, &full[s]);
+#pragma unroll
+        for (int k = 0; k < RPT; ++k) {
+          const int r = (lt >> 3) + k * (LDT / 8);
+          cp_async16(st + r * XP + ch * 16, xrow[k] + k0 + ch * 8, r < len ? nb : 0u);
+        }
+        if (lt == 0) mbar_arrive(&full[s]);
       }
-      mbar_arrive(&full[s]);
+      for (int j = lt >> 3; j < rank; j += LDT / 8)
+        cp_async16(st + (MBM + j) * XP + ch * 16, as + (int64_t)j * p.sa_row + k0 + ch * 8, nb);
+      cp_async_arrive(&full[s]);
     }
-    pdl_launch_dependents();
-    return;
-  }
-  if (warp == MCW + 1) {
-    // ---------------------------------------------------------------- storer (32 lanes)
-    constexpr int D = (NS - 1) < 2 ? (NS - 1) : 2;
-    int pend[D + 1];
-    int np = 0;
-    for (int g = 0; g < ntiles; ++g) {
-      const int s = g % NS;
-      if (!mbar_wait(&done[s], (g / NS) & 1)) break;
-      if (g < n1) {
-        if (lane == 0) mbar_arrive(&freeb[s]);
-        continue;
-      }
-      int i, c0, ocols;
-      blk(b_beg + g - n1, i, c0, ocols);
-      uint8_t *st = smem + s * C::STAGE;
-      for (int r = lane; r < len; r += 32)
-        bulk_store(p.y + (int64_t)p.perm[start + r] * p.ldy + c0, st + r * XP, ocols * 2);
-      bulk_commit();
-      pend[np++] = g;
-      if (np > D) {
-        bulk_wait_read_n<D>();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&freeb[pend[0] % NS]);
-        for (int k = 1; k < np; ++k) pend[k - 1] = pend[k];
-        --np;
-      }
-    }
-    bulk_wait_read_n<0>();
-    __syncwarp();
-    if (lane == 0)
-      for (int k = 0; k < np; ++k) mbar_arrive(&freeb[pend[k] % NS]);
-    bulk_wait_all();
     pdl_launch_dependents();
     return;
   }
 
   // ------------------------------------------------------------------ consumers
   const int w = warp, gq = lane >> 2, cq = lane & 3;
-  const bool rows_live = 16 * w < len;
-  float hacc[HC / 8][4];
+  const bool live = 16 * w < len;
+  float hacc[RP / 8][4];
 #pragma unroll
-  for (int i = 0; i < HC / 8; ++i) hacc[i][0] = hacc[i][1] = hacc[i][2] = hacc[i][3] = 0.f;
+  for (int t = 0; t < RP / 8; ++t) hacc[t][0] = hacc[t][1] = hacc[t][2] = hacc[t][3] = 0.f;
   bool ok = true;
-  int g = 0;
-  if (P1) {
-    for (; g < n1; ++g) {
+  const int l = lane_id();
+  for (int g = 0; g < k_end - k_beg; ++g) {
+    const int s = g % NS;
+    if (!(ok = wait_all(&full[s], (g / NS) & 1))) break;
+    const uint32_t xb = smem_u32(smem + s * C::STAGE), ab = xb + MBM * XP;
+    const int64_t k0 = (int64_t)(k_beg + g) * KW;
+    if (live) {
+#pragma unroll
+      for (int kk = 0; kk < KW / 16; ++kk) {
+        if (k0 + kk * 16 >= p.in) break;
+        uint32_t a[4];
+        const int ar = 16 * w + (l & 15), ac = kk * 16 + ((l >> 4) << 3);
+        ldsm_x4(xb + (dense ? swz_off(ar, ac) : (uint32_t)(ar * XP + ac * 2)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int np = 0; np < RP / 16; ++np) {
+          if (np * 16 >= rank) break;
+          uint32_t b[4];
+          ldb_p(ab, XP, np * 16, kk * 16, b);
+          mma_bf16(hacc[2 * np], a, b[0], b[1]);
+          mma_bf16(hacc[2 * np + 1], a, b[2], b[3]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+  // columns past the slot's rank come from unloaded (stale) rows of a: zero them
+#pragma unroll
+  for (int nt = 0; nt < RP / 8; ++nt) {
+    const int j = nt * 8 + 2 * cq;
+    if (j >= rank) hacc[nt][0] = hacc[nt][2] = 0.f;
+    if (j + 1 >= rank) hacc[nt][1] = hacc[nt][3] = 0.f;
+  }
+  const int r0 = 16 * w + gq;
+  if (cl > 1) {
+    named_bar_sync(1, SH_CWN * 32);   // every consumer warp is done with the ring
+#pragma unroll
+    for (int nt = 0; nt < RP / 8; ++nt) {
+      *reinterpret_cast<float2 *>(&hbuf[r0 * RP + nt * 8 + 2 * cq]) = make_float2(hacc[nt][0], hacc[nt][1]);
+      *reinterpret_cast<float2 *>(&hbuf[(r0 + 8) * RP + nt * 8 + 2 * cq]) = make_float2(hacc[nt][2], hacc[nt][3]);
+    }
+    for (int q = 0; q < cl; ++q)
+      if (q != (int)crank) mbar_arrive_remote(hready, q);
+    if (!wait_all<true>(hready, 0)) ok = false;
+    if (ok && live && (w % cl) == (int)crank) {
+#pragma unroll
+      for (int nt = 0; nt < RP / 8; ++nt) {
+        float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+        for (int q = 0; q < cl; ++q) {
+          float2 v0, v1;
+          if (q == (int)crank) {
+            v0 = make_float2(hacc[nt][0], hacc[nt][1]);
+            v1 = make_float2(hacc[nt][2], hacc[nt][3]);
+          } else {
+            v0 = ld_dsmem_f2(&hbuf[r0 * RP + nt * 8 + 2 * cq], q);
+            v1 = ld_dsmem_f2(&hbuf[(r0 + 8) * RP + nt * 8 + 2 * cq], q);
+          }
+          s0.x += v0.x; s0.y += v0.y; s1.x += v1.x; s1.y += v1.y;
+        }
+        hacc[nt][0] = s0.x; hacc[nt][1] = s0.y; hacc[nt][2] = s1.x; hacc[nt][3] = s1.y;
+      }
+    }
+    for (int q = 0; q < cl; ++q)
+      if (q != (int)crank) mbar_arrive_remote(hdone, q);
+  }
+  // h rows < len, columns j < rank of slice i; cluster CTA q writes the warps w % cl == q
+  if (ok && live && (w % cl) == (int)crank) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int r = r0 + 8 * hf;
+      if (r >= len) continue;
+      float *hrow = p.h + (int64_t)p.perm[start + r] * p.ldh + (int64_t)i * p.R;
+#pragma unroll
+      for (int nt = 0; nt < RP / 8; ++nt) {
+        const int j = nt * 8 + 2 * cq;
+        if (j + 1 < rank) {
+          *reinterpret_cast<float2 *>(&hrow[j]) = make_float2(hacc[nt][2 * hf], hacc[nt][2 * hf + 1]);
+        } else if (j < rank) {
+          hrow[j] = hacc[nt][2 * hf];
+        }
+      }
+    }
+  }
+  pdl_launch_dependents();
+  if (cl > 1) wait_all<true>(hdone, 0);   // peers are done reading this CTA's ring
+}
+
+// =============================================================================
+// expand_kernel: CTA (tile, group) adds slice i's product for the 64-column
+// blocks [b0, b0 + nb) of that slice:  y[t, c] += scal * sum_{j<rank} h[t, i*R+j] * b[slot][c][j].
+// Two loader warps fetch y (one TMA box for a full block of a dense tile, else
+// 64 gathered rows with 16-byte cp.async) and the slot's b rows (cp.async); two
+// storer warps write y back (one TMA store, or 16-byte stores per row).
+// =============================================================================
+constexpr int STW = 2;                 // storer warps
+constexpr int STT = STW * 32;
+
+template <int RP>
+struct ExCfg {
+  static constexpr int BPITCH = RP * 2 + 16;                       // b row pitch (bytes)
+  static constexpr int STAGE = ((MBM * XP + CBW * BPITCH) + 1023) / 1024 * 1024;
+  static constexpr int NS = (72 * 1024) / STAGE < 3 ? 3 : (72 * 1024) / STAGE > 6 ? 6 : (72 * 1024) / STAGE;
+  static constexpr int BYTES = 1024 + NS * STAGE + 8 * (3 * NS) + 64;
+  static constexpr int THREADS = (EX_CW + LDW + STW) * 32;
+};
+
+template <int RP>
+__global__ void __launch_bounds__(ExCfg<RP>::THREADS, RP >= 128 ? 2 : 3)
+    expand_kernel(const __grid_constant__ CUtensorMap tmY, MArgs p) {
+  using C = ExCfg<RP>;
+  constexpr int NS = C::NS;
+  constexpr int BP = C::BPITCH;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * C::STAGE);
+  uint64_t *done = full + NS;
+  uint64_t *freeb = done + NS;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x / p.ngroups, grp = blockIdx.x % p.ngroups;
+  pdl_wait();
+  if (tile >= p.header[1]) return;
+  // group -> (slice i, first block b0, number of blocks nb)
+  int i = 0, gleft = grp, b0 = 0, nb = 0;
+  for (; i < p.n; ++i) {
+    const int nblk = (p.off[i + 1] - p.off[i] + CBW - 1) / CBW;
+    const int ng = (nblk + p.gb - 1) / p.gb;
+    if (gleft < ng) {
+      b0 = gleft * p.gb;
+      nb = min(p.gb, nblk - b0);
+      break;
+    }
+    gleft -= ng;
+  }
+  if (i >= p.n || nb <= 0) return;
+  const int4 td = p.tiles[tile];
+  const int slot = td.x, start = td.y, len = td.z;
+  const int rank = p.ranks[slot];
+  const int rank8 = (rank + 7) & ~7;
+  const int col_end = p.off[i + 1];
+  const bool dense = (LORA_MULTI_TMA & 2) && p.tma_ok && dense_tile(p.perm, start, len);
+  const int t0 = p.perm[start];
+  // block g covers columns [c0, c0 + ocols); it moves by TMA when the tile is dense and the block full
+  auto block = [&](int g, int &c0, int &ocols) {
+    c0 = p.off[i] + (b0 + g) * CBW;
+    ocols = min(CBW, col_end - c0);
+    return dense && ocols == CBW;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], LDT + 1);
+      mbar_init(&done[s], EX_CW);
+      mbar_init(&freeb[s], STW);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp >= EX_CW && warp < EX_CW + LDW) {
+    // ---------------------------------------------------------------- loaders (64 threads)
+    const int lt = threadIdx.x - EX_CW * 32;
+    const int ch = lt & 7;
+    if (lt == 0 && dense) prefetch_tmap(&tmY);
+    __nv_bfloat16 *yrow[RPT];
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) {
+      const int r = (lt >> 3) + k * (LDT / 8);
+      yrow[k] = r < len ? p.y + (int64_t)p.perm[start + r] * p.ldy : p.y;
+    }
+    const __nv_bfloat16 *bs = p.b + (int64_t)slot * p.sb_slot;
+    const int bchunks = rank8 / 8;   // 16-byte chunks of a b row
+    for (int g = 0; g < nb; ++g) {
       const int s = g % NS;
-      if (!(ok = wait_all(&full[s], (g / NS) & 1))) break;
-      const uint32_t xb = smem_u32(smem + s * C::STAGE), ab = xb + MBM * XP;
-      const int64_t k0 = (int64_t)(k_beg + g) * KW;
-      if (rows_live) {
+      if (g >= NS && !mbar_wait(&freeb[s], ((g / NS) & 1) ^ 1)) break;
+      uint8_t *st = smem + s * C::STAGE;
+      int c0, ocols;
+      if (block(g, c0, ocols)) {
+        if (lt == 0) {
+          mbar_arrive_expect_tx(&full[s], MBM * CBW * 2);
+          tma_load_2d(st, &tmY, &full[s], c0, t0);
+        }
+      } else {
+        const uint32_t nbytes = clamp16(ocols * 2 - ch * 16);
 #pragma unroll
-        for (int kk = 0; kk < KW / 16; ++kk) {
-          if (k0 + kk * 16 >= p.in) break;
-          uint32_t a[4];
-          lda_p(xb, XP, 16 * w, kk * 16, a);
+        for (int k = 0; k < RPT; ++k) {
+          const int r = (lt >> 3) + k * (LDT / 8);
+          cp_async16(st + r * XP + ch * 16, yrow[k] + c0 + ch * 8, r < len ? nbytes : 0u);
+        }
+        if (lt == 0) mbar_arrive(&full[s]);
+      }
+      for (int it = lt; it < ocols * bchunks; it += LDT) {
+        const int cc = it / bchunks, q = it % bchunks;
+        cp_async16(st + MBM * XP + cc * BP + q * 16, bs + (int64_t)(c0 + cc) * p.sb_row + q * 8, 16u);
+      }
+      cp_async_arrive(&full[s]);
+    }
+    pdl_launch_dependents();
+    return;
+  }
+  if (warp >= EX_CW + LDW) {
+    // ---------------------------------------------------------------- storers (64 threads)
+    const int tt = threadIdx.x - (EX_CW + LDW) * 32;
+    const int ch = tt & 7;
+    const bool tma_lane = tt == 0;   // issues the TMA stores and releases their stages
+    constexpr int D = (NS - 1) < 2 ? (NS - 1) : 2;
+    int pend[D + 1];
+    int np = 0;
+    __nv_bfloat16 *yrow[RPT];
 #pragma unroll
-          for (int np = 0; np < HC / 16; ++np) {
-            if (np * 16 >= n * R) break;
-            uint32_t b[4];
-            ldb_p(ab, XP, np * 16, kk * 16, b);
-            mma_bf16(hacc[2 * np], a, b[0], b[1]);
-            mma_bf16(hacc[2 * np + 1], a, b[2], b[3]);
+    for (int k = 0; k < RPT; ++k) {
+      const int r = (tt >> 3) + k * (STT / 8);
+      yrow[k] = r < len ? p.y + (int64_t)p.perm[start + r] * p.ldy : p.y;
+    }
+    for (int g = 0; g < nb; ++g) {
+      const int s = g % NS;
+      if (!mbar_wait(&done[s], (g / NS) & 1)) break;
+      const uint8_t *st = smem + s * C::STAGE;
+      int c0, ocols;
+      if (block(g, c0, ocols)) {
+        if (tma_lane) {
+          tma_store_2d(&tmY, st, c0, t0);
+          bulk_commit();
+          pend[np++] = g;
+          if (np > D) {
+            bulk_wait_read<D>();
+            mbar_arrive(&freeb[pend[0] % NS]);
+            for (int k = 1; k < np; ++k) pend[k - 1] = pend[k];
+            --np;
+          }
+        } else if (lane == 0) {
+          mbar_arrive(&freeb[s]);     // the other storer warp has nothing to write
+        }
+      } else {
+        if (ch * 8 < ocols) {
+#pragma unroll
+          for (int k = 0; k < RPT; ++k) {
+            const int r = (tt >> 3) + k * (STT / 8);
+            if (r < len)
+              *reinterpret_cast<int4 *>(yrow[k] + c0 + ch * 8) = *reinterpret_cast<const int4 *>(st + r * XP + ch * 16);
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&freeb[s]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&done[s]);
     }
-    // columns past the slot's rank come from unloaded rows of a: zero them
-#pragma unroll
-    for (int nt = 0; nt < HC / 8; ++nt) {
-      const int c = nt * 8 + 2 * cq;
-      const bool v0 = c < n * R && (c % R) < rank, v1 = c + 1 < n * R && ((c + 1) % R) < rank;
-      if (!v0) hacc[nt][0] = hacc[nt][2] = 0.f;
-      if (!v1) hacc[nt][1] = hacc[nt][3] = 0.f;
+    if (tma_lane) {
+      bulk_wait_read<0>();
+      for (int k = 0; k < np; ++k) mbar_arrive(&freeb[pend[k] % NS]);
+      bulk_wait_all();
     }
-    if (cl > 1) {
-      // exchange partial h through distributed shared memory (in the stage ring)
-      named_bar_sync(1, MCW * 32);   // every consumer warp is done with the last phase-1 stage
-      const int r0 = 16 * w + gq;
+    pdl_launch_dependents();
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int w = warp, gq = lane >> 2, cq = lane & 3;
+  const bool live = 16 * w < len;
+  // slice i of h for rows 16w.., as bf16 A fragments; columns >= rank are zero.  One
+  // bf16 rounding of h (relative error 2^-9 per term) sits well inside what the
+  // bf16 result of the add can hold.
+  uint32_t ah[RP / 16][4];
+  {
+    float hv[RP / 8][4];
 #pragma unroll
-      for (int nt = 0; nt < HC / 8; ++nt) {
-        *reinterpret_cast<float2 *>(&hbuf[r0 * HC + nt * 8 + 2 * cq]) = make_float2(hacc[nt][0], hacc[nt][1]);
-        *reinterpret_cast<float2 *>(&hbuf[(r0 + 8) * HC + nt * 8 + 2 * cq]) = make_float2(hacc[nt][2], hacc[nt][3]);
-      }
-      for (int c = 0; c < cl; ++c)
-        if (c != (int)crank) mbar_arrive_remote(hready, c);
-      if (!wait_all<true>(hready, 0)) ok = false;
-      if (ok && rows_live) {
-#pragma unroll
-        for (int nt = 0; nt < HC / 8; ++nt) {
-          float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
-          for (int c = 0; c < cl; ++c) {
-            float2 v0, v1;
-            if (c == (int)crank) {
-              v0 = make_float2(hacc[nt][0], hacc[nt][1]);
-              v1 = make_float2(hacc[nt][2], hacc[nt][3]);
-            } else {
-              v0 = ld_dsmem_f2(&hbuf[r0 * HC + nt * 8 + 2 * cq], c);
-              v1 = ld_dsmem_f2(&hbuf[(r0 + 8) * HC + nt * 8 + 2 * cq], c);
-            }
-            s0.x += v0.x; s0.y += v0.y; s1.x += v1.x; s1.y += v1.y;
-          }
-          hacc[nt][0] = s0.x; hacc[nt][1] = s0.y; hacc[nt][2] = s1.x; hacc[nt][3] = s1.y;
-        }
-      }
-      for (int c = 0; c < cl; ++c)
-        if (c != (int)crank) mbar_arrive_remote(hdone, c);
-      wait_all<true>(hdone, 0);       // peers are done reading this CTA's part of the ring
-      mbar_arrive(xready);            // the loader may refill the ring
-    }
-    if (MODE == kShrink) {
-      // write h rows (< len) and columns j < rank; cluster CTA c writes the rows of warps w % cl == c
-      if (ok && rows_live && (w % cl) == (int)crank) {
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int r = 16 * w + gq + 8 * hf;
-          if (r >= len) continue;
-          float *hrow = p.h + (int64_t)p.perm[start + r] * p.ldh;
-#pragma unroll
-          for (int nt = 0; nt < HC / 8; ++nt) {
-            const int c = nt * 8 + 2 * cq;
-            if (c < n * R && (c % R) < rank) hrow[c] = hacc[nt][2 * hf];
-            if (c + 1 < n * R && ((c + 1) % R) < rank) hrow[c + 1] = hacc[nt][2 * hf + 1];
-          }
-        }
-      }
-      pdl_launch_dependents();
-      return;
-    }
-  } else {
-    // expand: h rows of the tile from global memory (columns past the rank are masked)
-    if (rows_live) {
+    for (int nt = 0; nt < RP / 8; ++nt) hv[nt][0] = hv[nt][1] = hv[nt][2] = hv[nt][3] = 0.f;
+    if (live) {
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int r = 16 * w + gq + 8 * hf;
         if (r >= len) continue;
-        const float *hrow = p.h + (int64_t)p.perm[start + r] * p.ldh;
+        const float *hrow = p.h + (int64_t)p.perm[start + r] * p.ldh + (int64_t)i * p.R;
 #pragma unroll
-        for (int nt = 0; nt < HC / 8; ++nt) {
-          const int c = nt * 8 + 2 * cq;
-          if (c < n * R && (c % R) < rank) hacc[nt][2 * hf] = __ldg(&hrow[c]);
-          if (c + 1 < n * R && ((c + 1) % R) < rank) hacc[nt][2 * hf + 1] = __ldg(&hrow[c + 1]);
+        for (int nt = 0; nt < RP / 8; ++nt) {
+          const int j = nt * 8 + 2 * cq;
+          if (j < rank) hv[nt][2 * hf] = __ldg(&hrow[j]);
+          if (j + 1 < rank) hv[nt][2 * hf + 1] = __ldg(&hrow[j + 1]);
         }
       }
     }
-  }
-
-  // ------------------------------------------------------------------ phase 2
-  uint32_t ahi[HC / 16][4], alo[HC / 16][4];
 #pragma unroll
-  for (int q = 0; q < HC / 16; ++q) {
-    split_bf16(hacc[2 * q][0], hacc[2 * q][1], ahi[q][0], alo[q][0]);
-    split_bf16(hacc[2 * q][2], hacc[2 * q][3], ahi[q][1], alo[q][1]);
-    split_bf16(hacc[2 * q + 1][0], hacc[2 * q + 1][1], ahi[q][2], alo[q][2]);
-    split_bf16(hacc[2 * q + 1][2], hacc[2 * q + 1][3], ahi[q][3], alo[q][3]);
+    for (int q = 0; q < RP / 16; ++q) {
+      ah[q][0] = pack_bf16(hv[2 * q][0], hv[2 * q][1]);
+      ah[q][1] = pack_bf16(hv[2 * q][2], hv[2 * q][3]);
+      ah[q][2] = pack_bf16(hv[2 * q + 1][0], hv[2 * q + 1][1]);
+      ah[q][3] = pack_bf16(hv[2 * q + 1][2], hv[2 * q + 1][3]);
+    }
   }
   const float sc = p.scal[slot];
-  for (; ok && g < ntiles; ++g) {
+  for (int g = 0; g < nb; ++g) {
     const int s = g % NS;
-    if (!(ok = wait_all(&full[s], (g / NS) & 1))) break;
+    if (!wait_all(&full[s], (g / NS) & 1)) break;
     uint8_t *st = smem + s * C::STAGE;
-    if (rows_live) {
-      int i, c0, ocols;
-      blk(b_beg + g - n1, i, c0, ocols);
+    int c0, ocols;
+    const bool tmab = block(g, c0, ocols);
+    if (live) {
       const uint32_t bb = smem_u32(st) + MBM * XP;
       float acc[8][4];
 #pragma unroll
       for (int t = 0; t < 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-      const int cs = i * R;   // first h column of slice i
 #pragma unroll
-      for (int q = 0; q < HC / 16; ++q) {
-        if (q * 16 < cs || q * 16 >= cs + rank) continue;
-        const int j0 = q * 16 - cs;
+      for (int q = 0; q < RP / 16; ++q) {
+        if (q * 16 >= rank) break;
+        const int j0 = q * 16;
+        const bool part = j0 + 16 > rank;   // the b padding past the rank (any value) is masked
 #pragma unroll
         for (int np = 0; np < 4; ++np) {
           uint32_t b[4];
-          ldb_p(bb, bp, np * 16, j0, b);
-          b[0] = mask_pair(b[0], j0 + 2 * cq, rank);
-          b[1] = mask_pair(b[1], j0 + 8 + 2 * cq, rank);
-          b[2] = mask_pair(b[2], j0 + 2 * cq, rank);
-          b[3] = mask_pair(b[3], j0 + 8 + 2 * cq, rank);
-          mma_bf16(acc[2 * np], ahi[q], b[0], b[1]);
-          mma_bf16(acc[2 * np], alo[q], b[0], b[1]);
-          mma_bf16(acc[2 * np + 1], ahi[q], b[2], b[3]);
-          mma_bf16(acc[2 * np + 1], alo[q], b[2], b[3]);
+          ldb_p(bb, BP, np * 16, j0, b);
+          if (part) {
+            b[0] = mask_pair(b[0], j0 + 2 * cq, rank);
+            b[1] = mask_pair(b[1], j0 + 8 + 2 * cq, rank);
+            b[2] = mask_pair(b[2], j0 + 2 * cq, rank);
+            b[3] = mask_pair(b[3], j0 + 8 + 2 * cq, rank);
+          }
+          mma_bf16(acc[2 * np], ah[q], b[0], b[1]);
+          mma_bf16(acc[2 * np + 1], ah[q], b[2], b[3]);
         }
       }
 #pragma unroll
@@ -526,13 +706,13 @@ __global__ void __launch_bounds__(MTHREADS) seg_kernel(SegArgs p) {
         for (int hf = 0; hf < 2; ++hf) {
           const int r = 16 * w + gq + 8 * hf;
           if (r >= len) continue;
-          uint32_t *yp = reinterpret_cast<uint32_t *>(st + r * XP + cc * 2);
+          uint32_t *yp = reinterpret_cast<uint32_t *>(st + (tmab ? swz_off(r, cc) : (uint32_t)(r * XP + cc * 2)));
           const float2 yv = unpack_bf16(*yp);
           *yp = pack_bf16(yv.x + sc * acc[nt][2 * hf], yv.y + sc * acc[nt][2 * hf + 1]);
         }
       }
     }
-    fence_proxy_async_smem();
+    if (tmab) fence_proxy_async_smem();   // the TMA store reads what these threads wrote
     __syncwarp();
     if (lane == 0) mbar_arrive(&done[s]);
   }
@@ -565,6 +745,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t *__restrict__
   pdl_launch_dependents();
 }
 
+
 // ----------------------------------------------------------------------------- host side
 namespace {
 
@@ -580,6 +761,8 @@ size_t sched_bytes(int64_t T, int S) {
   return ws_round(256) + ws_round((size_t)S * 4) + ws_round((size_t)std::max<int64_t>(T, 1) * 4) +
          ws_round((size_t)max_tiles(T, S) * 16);
 }
+// h of apply_linear, kept between its two kernels (n * R <= kMaxHC columns)
+size_t hbuf_bytes(int64_t T, int R) { return ws_round((size_t)T * std::min(kMaxHC, LORA_MAX_SLICES * R) * 4); }
 
 bool carve_sched(WsCarver &c, int64_t T, int S, SchedPtrs &sp) {
   sp.header = (int *)c.take(256);
@@ -592,48 +775,85 @@ bool carve_sched(WsCarver &c, int64_t T, int S, SchedPtrs &sp) {
 lora_status_t launch_group(const lora_addressing_t &ad, const int32_t *ranks, int32_t *counts, int32_t *perm,
                            int32_t *num_active, int *header, int4 *tiles, cudaStream_t st) {
   const int S = ad.num_slots;
-  int nw = (int)std::min<int64_t>(32, std::max<int64_t>(1, (160 * 1024 / 4 - 256) / S));
+  int nw = (int)std::max<int64_t>(1, (160 * 1024 / 4 - 256 - S) / S);
   nw = std::min(nw, 32);
-  const size_t smem = (size_t)(nw * S + 160) * 4;
+  const size_t smem = (size_t)(nw * S + S + 160) * 4;
   LORA_CUDA(ensure_smem((const void *)group_kernel, smem));
   LORA_CUDA(launch(group_kernel, dim3(1), dim3(nw * 32), smem, st, 1, true, ad.slots, ad.num_tokens, S,
                    ad.max_rank, ranks, counts, perm, num_active, header, tiles, (int)MBM));
   return LORA_OK;
 }
 
-template <int HC, int MODE>
-lora_status_t launch_seg(SegArgs a, int64_t T, cudaStream_t st) {
-  auto kern = seg_kernel<HC, MODE>;
-  const size_t smem = SegCfg<HC>::BYTES;
+// 64 x 64 bf16 tiles of a row-major [rows][cols] operand (128-byte swizzle).
+bool map_rows(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld) {
+  uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+  uint64_t str[1] = {(uint64_t)ld * 2};
+  uint32_t box[2] = {64, 64};
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int RP>
+lora_status_t launch_shrink(MArgs a, int64_t T, cudaStream_t st) {
+  auto kern = shrink_kernel<RP>;
+  const size_t smem = ShCfg<RP>::BYTES;
   LORA_CUDA(ensure_smem((const void *)kern, smem));
-  const int occ = occupancy((const void *)kern, MTHREADS, smem);
-  const int64_t tiles = max_tiles(T, a.S);
-  const int64_t cap = (int64_t)occ * num_sms();
+  CUtensorMap tmX;
+  a.tma_ok = map_rows(&tmX, a.x, T, a.in, a.ldx) ? 1 : 0;
+  const int occ = occupancy((const void *)kern, ShCfg<RP>::THREADS, smem);
+  const int64_t items = (int64_t)max_tiles(T, a.S) * a.n, cap = (int64_t)occ * num_sms();
   int cl = 1;
-  while (cl * 2 <= 8 && tiles * cl * 2 <= cap) cl *= 2;
-  if (MODE != kExpand)
-    while (cl > 1 && ceil_div(a.in, KW) < cl) cl /= 2;
-  if (MODE != kShrink)
-    while (cl > 1 && a.nb < cl) cl /= 2;
+  while (cl * 2 <= 8 && items * cl * 2 <= cap) cl *= 2;
+  while (cl > 1 && ceil_div(a.in, KW) < cl) cl /= 2;
   a.cl = cl;
-  LORA_CUDA(launch(kern, dim3((unsigned)(tiles * cl)), dim3(MTHREADS), smem, st, cl, true, a));
+  LORA_CUDA(launch(kern, dim3((unsigned)(items * cl)), dim3(ShCfg<RP>::THREADS), smem, st, cl, true, tmX, a));
   return LORA_OK;
 }
 
-template <int MODE>
-lora_status_t dispatch_seg(SegArgs a, int64_t T, cudaStream_t st) {
-  const int hc = a.n * a.R;
-  if (hc <= 64) return launch_seg<64, MODE>(a, T, st);
-  if (hc <= 128) return launch_seg<128, MODE>(a, T, st);
-  if (hc <= 192) return launch_seg<192, MODE>(a, T, st);
-  return launch_seg<256, MODE>(a, T, st);
+lora_status_t dispatch_shrink(const MArgs &a, int64_t T, cudaStream_t st) {
+  switch (rank_bucket(a.R)) {
+    case 16: return launch_shrink<16>(a, T, st);
+    case 32: return launch_shrink<32>(a, T, st);
+    case 64: return launch_shrink<64>(a, T, st);
+    default: return launch_shrink<128>(a, T, st);
+  }
 }
 
-// Shared argument checks of the segmented ops (beyond those of the ABI layer).
+template <int RP>
+lora_status_t launch_expand(MArgs a, int64_t T, cudaStream_t st) {
+  auto kern = expand_kernel<RP>;
+  const size_t smem = ExCfg<RP>::BYTES;
+  LORA_CUDA(ensure_smem((const void *)kern, smem));
+  const int occ = occupancy((const void *)kern, ExCfg<RP>::THREADS, smem);
+  const int64_t tiles = max_tiles(T, a.S), cap = (int64_t)occ * num_sms();
+  int64_t blocks = 0;
+  for (int i = 0; i < a.n; ++i) blocks += ceil_div(a.off[i + 1] - a.off[i], CBW);
+  // column blocks per CTA: about three waves of CTAs over the tile bound
+  const int64_t gb = std::max<int64_t>(1, ceil_div(tiles * blocks, 3 * cap));
+  int64_t ng = 0;
+  for (int i = 0; i < a.n; ++i) ng += ceil_div(ceil_div(a.off[i + 1] - a.off[i], CBW), gb);
+  if (ng == 0) return LORA_OK;
+  a.gb = (int)gb;
+  a.ngroups = (int)ng;
+  CUtensorMap tmY;
+  a.tma_ok = map_rows(&tmY, a.y, T, a.off[a.n], a.ldy) ? 1 : 0;
+  LORA_CUDA(launch(kern, dim3((unsigned)(tiles * ng)), dim3(ExCfg<RP>::THREADS), smem, st, 1, true, tmY, a));
+  return LORA_OK;
+}
+
+lora_status_t dispatch_expand(const MArgs &a, int64_t T, cudaStream_t st) {
+  switch (rank_bucket(a.R)) {
+    case 16: return launch_expand<16>(a, T, st);
+    case 32: return launch_expand<32>(a, T, st);
+    case 64: return launch_expand<64>(a, T, st);
+    default: return launch_expand<128>(a, T, st);
+  }
+}
+
+// Argument checks of the segmented ops beyond those of the ABI layer.
 lora_status_t check_seg(const MultiArgs &m, bool need_in, bool need_out) {
   const int R = m.addr.max_rank;
   if ((int64_t)m.n * R > kMaxHC) return LORA_ERR_UNSUPPORTED;
-  if (R % 8 != 0 || (m.n > 1 && R % 16 != 0)) return LORA_ERR_UNSUPPORTED;
+  if (R % 8 != 0) return LORA_ERR_UNSUPPORTED;
   if (need_in && m.in % 8 != 0) return LORA_ERR_UNSUPPORTED;
   if (need_out) {
     for (int i = 0; i < m.n; ++i)
@@ -644,15 +864,13 @@ lora_status_t check_seg(const MultiArgs &m, bool need_in, bool need_out) {
   return LORA_OK;
 }
 
-SegArgs seg_args(const MultiArgs &m, const SchedPtrs &sp) {
-  SegArgs a{};
-  a.slots = m.addr.slots;
+MArgs margs(const MultiArgs &m, const SchedPtrs &sp) {
+  MArgs a{};
   a.ranks = m.ranks;
   a.scal = m.scalings;
   a.header = sp.header;
   a.tiles = sp.tiles;
   a.perm = sp.perm;
-  a.T = m.addr.num_tokens;
   a.S = m.addr.num_slots;
   a.R = m.addr.max_rank;
   a.n = m.n;
@@ -669,17 +887,18 @@ SegArgs seg_args(const MultiArgs &m, const SchedPtrs &sp) {
   a.ldh = m.ldh;
   a.y = (__nv_bfloat16 *)m.y;
   a.ldy = m.ldy;
-  int off = 0, nb = 0;
+  int off = 0;
   for (int i = 0; i < m.n; ++i) {
     a.off[i] = off;
-    a.blk0[i] = nb;
     off += m.out_slices[i];
-    nb += (m.out_slices[i] + CBW - 1) / CBW;
   }
   a.off[m.n] = off;
-  a.blk0[m.n] = nb;
-  a.nb = nb;
   return a;
+}
+
+lora_status_t schedule(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, cudaStream_t st) {
+  if (!carve_sched(c, m.addr.num_tokens, m.addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
+  return launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st);
 }
 
 }  // namespace
@@ -687,51 +906,54 @@ SegArgs seg_args(const MultiArgs &m, const SchedPtrs &sp) {
 size_t multi_ws_bytes(int op, int64_t T, int64_t in, int64_t O, int R, int S) {
   (void)in;
   (void)O;
-  (void)R;
-  if (op == LORA_OP_GROUP_BY_SLOT || op == LORA_OP_SHRINK || op == LORA_OP_EXPAND || op == LORA_OP_APPLY_LINEAR)
-    return T > 0 ? sched_bytes(T, S) : 0;
+  if (T <= 0) return 0;
+  if (op == LORA_OP_GROUP_BY_SLOT || op == LORA_OP_SHRINK || op == LORA_OP_EXPAND) return sched_bytes(T, S);
+  if (op == LORA_OP_APPLY_LINEAR) return sched_bytes(T, S) + hbuf_bytes(T, R);
   return 0;
 }
 
 lora_status_t group_by_slot(const lora_addressing_t &addr, const int32_t *ranks, int32_t *counts, int32_t *perm,
                             int32_t *num_active, void *ws, size_t ws_bytes, cudaStream_t st) {
-  WsCarver c(ws, ws_bytes);
-  SchedPtrs sp;
-  if (addr.num_tokens > 0 && !carve_sched(c, addr.num_tokens, addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
   if (addr.num_tokens == 0) {
-    // no tokens: counts are zero, no active tokens
+    // no tokens: every count is zero and no token is active
     LORA_CUDA(cudaMemsetAsync(counts, 0, (size_t)addr.num_slots * 4, st));
     LORA_CUDA(cudaMemsetAsync(num_active, 0, 4, st));
     return LORA_OK;
   }
-  return launch_group(addr, ranks, counts, perm, num_active, sp.header, sp.tiles, st);
-}
-
-static lora_status_t schedule(const MultiArgs &m, void *ws, size_t ws_bytes, SchedPtrs &sp, cudaStream_t st) {
   WsCarver c(ws, ws_bytes);
-  if (!carve_sched(c, m.addr.num_tokens, m.addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
-  return launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st);
+  SchedPtrs sp;
+  if (!carve_sched(c, addr.num_tokens, addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
+  return launch_group(addr, ranks, counts, perm, num_active, sp.header, sp.tiles, st);
 }
 
 lora_status_t shrink(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t st) {
   LORA_TRY(check_seg(m, true, false));
+  WsCarver c(ws, ws_bytes);
   SchedPtrs sp;
-  LORA_TRY(schedule(m, ws, ws_bytes, sp, st));
-  return dispatch_seg<kShrink>(seg_args(m, sp), m.addr.num_tokens, st);
+  LORA_TRY(schedule(m, c, sp, st));
+  return dispatch_shrink(margs(m, sp), m.addr.num_tokens, st);
 }
 
 lora_status_t expand(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t st) {
   LORA_TRY(check_seg(m, false, true));
+  WsCarver c(ws, ws_bytes);
   SchedPtrs sp;
-  LORA_TRY(schedule(m, ws, ws_bytes, sp, st));
-  return dispatch_seg<kExpand>(seg_args(m, sp), m.addr.num_tokens, st);
+  LORA_TRY(schedule(m, c, sp, st));
+  return dispatch_expand(margs(m, sp), m.addr.num_tokens, st);
 }
 
 lora_status_t apply_linear(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t st) {
   LORA_TRY(check_seg(m, true, true));
+  WsCarver c(ws, ws_bytes);
   SchedPtrs sp;
-  LORA_TRY(schedule(m, ws, ws_bytes, sp, st));
-  return dispatch_seg<kApply>(seg_args(m, sp), m.addr.num_tokens, st);
+  LORA_TRY(schedule(m, c, sp, st));
+  float *h = (float *)c.take(hbuf_bytes(m.addr.num_tokens, m.addr.max_rank));
+  if (!h) return LORA_ERR_WORKSPACE;
+  MArgs a = margs(m, sp);
+  a.h = h;
+  a.ldh = (int64_t)m.n * m.addr.max_rank;
+  LORA_TRY(dispatch_shrink(a, m.addr.num_tokens, st));
+  return dispatch_expand(a, m.addr.num_tokens, st);
 }
 
 lora_status_t gather_shrink(MultiArgs m, cudaStream_t st) {
