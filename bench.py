@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma-separated op names to run (profiling); default: all")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA-graph replays")
     return ap.parse_args()
 
 
@@ -331,6 +332,22 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def reduce_max(value, device):
+    """Max of a float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank, world, ms_per_step_max):
+    """Whole-job tokens/s: every rank processes its own batch; the slowest rank sets the time."""
+    return world * tokens_per_rank / (ms_per_step_max / 1e3)
+
+
 def traffic_from_profiles(kernel_key):
     """Per-launch DRAM bytes of `kernel_key` from the committed ncu summary, if the
     kernel source it was taken from is unchanged (else None)."""
@@ -394,12 +411,42 @@ def run_gb300(args, rank, world, local_rank):
     torch.cuda.synchronize()
     assert lora.lora_device_error() == 0
 
+    # one CUDA graph per input-set rotation: a step's launches (with their
+    # programmatic-dependent-launch edges) replay without host overhead
+    graphs = None
+    if not args.no_graph:
+        try:
+            graphs = []
+            cap_stream = torch.cuda.Stream()
+            cap_stream.wait_stream(stream)
+            with torch.cuda.stream(cap_stream):
+                for j in range(NSETS):
+                    step(j)                       # warm the capture stream
+                torch.cuda.synchronize()
+                for j in range(NSETS):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=cap_stream):
+                        step(j)
+                    graphs.append(g)
+            torch.cuda.synchronize()
+            for i in range(max(args.warmup, 3)):
+                graphs[i % NSETS].replay()
+            torch.cuda.synchronize()
+        except Exception as exc:                  # capture unsupported: time eager launches
+            sys.stderr.write(f"CUDA graph capture failed ({exc}); timing eager launches\n")
+            graphs = None
+            torch.cuda.synchronize()
+
+    def run_step(i):
+        if graphs is not None:
+            graphs[i % NSETS].replay()
+        else:
+            step(i)
+
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.35)
     K = args.steps
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
-           for _ in range(K)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
@@ -407,26 +454,37 @@ def run_gb300(args, rank, world, local_rank):
     t_host0 = time.time()
     e0.record(stream)
     for i in range(K):
-        step(i, evs[i])
+        run_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     t_host1 = time.time()
     barrier()
+    # graph replays do not pass through the library's launch counter: count one
+    # step's launches eagerly and scale
     launches = lora.lora_kernel_launches() - launches0
+    if graphs is not None:
+        c0 = lora.lora_kernel_launches()
+        step(0)
+        torch.cuda.synchronize()
+        launches = (lora.lora_kernel_launches() - c0) * K
     time.sleep(0.25)
     sampler.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(e0.elapsed_time(e1), dev)
     ms_per_step = ms / K
-    value = world * tokens / (ms_per_step / 1e3)
+    value = weak_scaling_value(tokens, world, ms_per_step)
+
+    # per-op device times (eager launches, events around each op, same rotation)
+    KP = max(10, min(K, 200))
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
+           for _ in range(KP)]
+    for i in range(KP):
+        step(i, evs[i])
+    torch.cuda.synchronize()
 
     peak, peak_kind = peaks()
     parts = {}
     for j, (name, _, nbytes) in enumerate(ops):
-        t_ms = statistics.mean(evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(K))
+        t_ms = statistics.mean(evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(KP))
         gbs = nbytes / (t_ms / 1e3) / 1e9
         parts[name] = {"ms": t_ms, "bytes": nbytes, "GB/s": gbs, "frac_of_" + peak_kind: gbs / peak,
                        "tokens/s": tokens / (t_ms / 1e3)}
@@ -467,11 +525,7 @@ def run_gb300(args, rank, world, local_rank):
             e2e_step(i)
         f1.record(stream)
         torch.cuda.synchronize()
-        e_ms = f0.elapsed_time(f1) / E
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = reduce_max(f0.elapsed_time(f1) / E, dev)
     assert lora.lora_device_error() == 0
 
     cpu = None
@@ -485,10 +539,11 @@ def run_gb300(args, rank, world, local_rank):
                 "data": "synthetic (seeded SplitMix64; inputs resident in HBM)",
                 "config": {"workload": WORKLOAD, "model": "q_proj LoRA (Llama-like 4096)", "global_batch": 8192 * world,
                            "seq_len": 2048, "parallelism": f"replicas x{world}",
-                           "l2": f"{NSETS} rotating input sets, each > L2; consecutive ops use different sets"},
+                           "l2": f"{NSETS} rotating input sets, each > L2; consecutive ops use different sets",
+                           "launch": "eager" if graphs is None else "CUDA graph per step (PDL edges kept)"},
                 "parts": parts, "roofline": roof, "cpu_baseline": cpu,
                 "e2e": None if e_ms is None else {
-                    "value": world * tokens / (e_ms / 1e3), "unit": UNIT, "steps": E,
+                    "value": weak_scaling_value(tokens, world, e_ms), "unit": UNIT, "steps": E,
                     "h2d_bytes_per_step": h2d * sets_per_step, "d2h_bytes_per_step": d2h * sets_per_step},
                 "gpu_launches": int(launches), "clocks": sampler.summary(t_host0, t_host1)}
         print(json.dumps(line), flush=True)

@@ -226,9 +226,10 @@ LORA_API lora_status_t lora_expand(const lora_addressing_t *addr, const int32_t 
                           void *ws, size_t ws_bytes, void *stream);
 
 /* --------------------------------------------------------------------------------
- * lora_apply_linear: shrink then expand into y, fused ([mstar lora.ops]
- * apply_linear_: "a backend may fuse them"); h never leaves the chip.
- * Arguments as in lora_shrink / lora_expand.
+ * lora_apply_linear: shrink then expand into y in one call ([mstar lora.ops]
+ * apply_linear_).  The two kernels share one device-built schedule and are
+ * chained with programmatic dependent launch; h passes between them through the
+ * workspace (it stays in L2).  Arguments as in lora_shrink / lora_expand.
  * -------------------------------------------------------------------------------- */
 LORA_API lora_status_t lora_apply_linear(const lora_addressing_t *addr, const int32_t *ranks,
                                 const float *scalings, const int32_t *out_slices, int32_t num_slices,

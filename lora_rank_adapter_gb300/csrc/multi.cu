@@ -163,6 +163,10 @@ __device__ __forceinline__ void block_scan2(int a, int b, int &ea, int &eb, int 
 }
 
 constexpr int GU = 8;   // tokens per lane per batch in group_kernel
+// Tokens per warp the grouping aims for (fewer warps: shorter scans and barriers).
+#ifndef LORA_GROUP_TOKENS_PER_WARP
+#define LORA_GROUP_TOKENS_PER_WARP 256
+#endif
 
 __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__ slots, int T, int S, int R,
                                                      const int32_t *__restrict__ ranks, int32_t *counts_out,
@@ -775,8 +779,8 @@ bool carve_sched(WsCarver &c, int64_t T, int S, SchedPtrs &sp) {
 lora_status_t launch_group(const lora_addressing_t &ad, const int32_t *ranks, int32_t *counts, int32_t *perm,
                            int32_t *num_active, int *header, int4 *tiles, cudaStream_t st) {
   const int S = ad.num_slots;
-  int nw = (int)std::max<int64_t>(1, (160 * 1024 / 4 - 256 - S) / S);
-  nw = std::min(nw, 32);
+  int nw = (int)std::max<int64_t>(1, (160 * 1024 / 4 - 256 - S) / S);   // shared-memory bound
+  nw = std::min<int64_t>({nw, 32, std::max<int64_t>(1, ceil_div(ad.num_tokens, LORA_GROUP_TOKENS_PER_WARP))});
   const size_t smem = (size_t)(nw * S + S + 160) * 4;
   LORA_CUDA(ensure_smem((const void *)group_kernel, smem));
   LORA_CUDA(launch(group_kernel, dim3(1), dim3(nw * 32), smem, st, 1, true, ad.slots, ad.num_tokens, S,
