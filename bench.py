@@ -389,7 +389,11 @@ def run_gb300(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     sets, ops, tokens = make_ops(torch, lora, binding, synth, dev)
     if args.only:
-        keep = set(args.only.split(","))
+        # names with or without the "lora_" prefix
+        keep = {k if k.startswith("lora_") else "lora_" + k for k in args.only.split(",")}
+        unknown = keep - {op[0] for op in ops}
+        if unknown:
+            raise SystemExit(f"--only: unknown op(s) {sorted(unknown)}; known: {[op[0] for op in ops]}")
         ops = [op for op in ops if op[0] in keep]
     torch.cuda.synchronize()
 

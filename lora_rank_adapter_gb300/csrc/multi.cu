@@ -10,7 +10,7 @@
 // slot, built on the device with no host sync (the page requires the ops to run
 // without one).
 //
-// shrink_kernel: one (token tile, slice) per cluster of `cl` CTAs; the
+// shrink_kernel: one token tile (all slices) per cluster of `cl` CTAs; the
 // contraction is split over the cluster and the partial h are summed in
 // cluster-rank order through distributed shared memory.
 // expand_kernel: one (token tile, slice, group of 64-column blocks) per CTA;
@@ -18,8 +18,8 @@
 // a loader and a storer warp.
 // apply_linear runs both, chained by programmatic dependent launch, with h in
 // the workspace (it stays in L2 between the two kernels).
-// Rows are gathered (a tile's tokens need not be contiguous) with one 1-D bulk
-// copy per row into padded shared-memory rows (conflict-free ldmatrix).
+// Rows of a tile whose tokens are not consecutive are gathered with 16-byte
+// cp.async copies; consecutive rows and the adapter rows move as TMA boxes.
 // Adapter padding (rows / columns past a slot's rank, which may hold anything)
 // is masked in registers, never trusted.
 #include <algorithm>
@@ -55,6 +55,12 @@ struct MArgs {
   __nv_bfloat16 *y; int64_t ldy;
   int off[LORA_MAX_SLICES + 1];   // output column offset of each slice
   int tma_ok;                     // the tensor maps of x / y are valid
+  int tma_a;                      // the tensor map of a is valid (shrink)
+  int sh_ns, sh_stage;            // shrink: stages in the ring, bytes per stage
+  int sh_nc, nk;                  // shrink: partial-sum row pitch (columns), stages per tile
+  const int2 *starts;             // shrink: first (tile, stage) of each CTA, [G + 1]
+  int *tickets;                   // shrink: stages finished per tile
+  float *part;                    // shrink: partial sums, [2 G][64][sh_nc]
 };
 
 // Byte offset of (row, col) in a 64 x 64 bf16 tile written by TMA with the
@@ -86,10 +92,21 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                : "memory");
 }
 
-// Warp-uniform bounded wait.
+// Warp-uniform bounded wait: lane 0 polls the barrier, the warp barrier then
+// orders what lane 0 observed before every lane's later reads.
+#ifndef LORA_POLL_ONE
+#define LORA_POLL_ONE 1
+#endif
 template <bool kCluster = false>
 __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
+#if LORA_POLL_ONE
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait<kCluster>(bar, parity);
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+#else
   return __all_sync(0xffffffffu, mbar_wait<kCluster>(bar, parity));
+#endif
 }
 
 // A operand (16x16 at rows r0.., cols c0..) / B operands (two n8 tiles) from padded rows.
@@ -163,6 +180,16 @@ __device__ __forceinline__ void block_scan2(int a, int b, int &ea, int &eb, int 
 }
 
 constexpr int GU = 8;   // tokens per lane per batch in group_kernel
+
+// Optional output of the grouping for the shrink: the split of its work over G
+// persistent CTAs.  Tile tau costs nk stages of n * rank16(slot) + 64 rows of
+// 128 bytes (a rows of every slice plus x rows); CTA b starts at the first
+// (tile, stage) whose cost offset is at least floor(total * b / G).
+struct SplitOut {
+  int2 *starts;    // [G + 1] (tile, stage); starts[G] = (tiles, 0)
+  int *tickets;    // [ntick] zeroed: stages of a tile finished so far
+  int G, n, nk, ntick;
+};
 // Tokens per warp the grouping aims for (fewer warps: shorter scans and barriers).
 #ifndef LORA_GROUP_TOKENS_PER_WARP
 #define LORA_GROUP_TOKENS_PER_WARP 256
@@ -171,12 +198,14 @@ constexpr int GU = 8;   // tokens per lane per batch in group_kernel
 __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__ slots, int T, int S, int R,
                                                      const int32_t *__restrict__ ranks, int32_t *counts_out,
                                                      int32_t *perm_out, int32_t *num_active_out, int *header,
-                                                     int4 *tiles, int bmt) {
+                                                     int4 *tiles, int bmt, SplitOut so) {
   extern __shared__ int gsm[];
   const int nw = blockDim.x >> 5;
   int *hist = gsm;                 // [nw][S]
   int *srank = gsm + nw * S;       // [S]
   int *sh = srank + S;             // scan scratch (160 ints)
+  int *stb = sh + 160;             // [S] first tile of each slot
+  int *spc = stb + S;              // [S + 1] cost prefix of each slot (per stage)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
   const int t_lo = (int)((int64_t)T * warp / nw), t_hi = (int)((int64_t)T * (warp + 1) / nw);
@@ -209,7 +238,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
     }
   }
   __syncthreads();
-  int run = 0, trun = 0;
+  int run = 0, trun = 0, crun = 0;
   for (int c0 = 0; c0 < S; c0 += blockDim.x) {
     const int s = c0 + threadIdx.x;
     int cnt = 0;
@@ -228,9 +257,46 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
         cur += hcount;
       }
       for (int i = 0; i < nt; ++i) tiles[tb + i] = make_int4(s, base + i * bmt, min(bmt, cnt - i * bmt), 0);
+      stb[s] = tb;
     }
     run += tc;
     trun += tt;
+    if (so.G > 0) {
+      const int cost = s < S ? nt * (so.n * ((srank[s] + 15) & ~15) + 64) : 0;
+      int ecost, dummy, tcost, tdummy;
+      block_scan2(cost, 0, ecost, dummy, tcost, tdummy, sh);
+      if (s < S) spc[s] = crun + ecost;
+      crun += tcost;
+    }
+  }
+  if (so.G > 0) {
+    if (threadIdx.x == 0) spc[S] = crun;
+    for (int i = threadIdx.x; i < so.ntick; i += blockDim.x) so.tickets[i] = 0;
+    __syncthreads();
+    const int64_t total = (int64_t)crun * so.nk;
+    for (int b = threadIdx.x; b <= so.G; b += blockDim.x) {
+      const int64_t c = total * b / so.G;
+      int tau = trun, k = 0;
+      if (c < total) {
+        int lo = 0, hi = S - 1;   // the last slot whose cost starts at or before c
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if ((int64_t)spc[mid] * so.nk <= c) lo = mid;
+          else hi = mid - 1;
+        }
+        const int64_t w = so.n * ((srank[lo] + 15) & ~15) + 64;
+        const int64_t o = c - (int64_t)spc[lo] * so.nk;
+        int64_t ti = o / (so.nk * w);
+        int64_t kk = (o - ti * so.nk * w + w - 1) / w;
+        if (kk >= so.nk) {
+          ++ti;
+          kk = 0;
+        }
+        tau = stb[lo] + (int)ti;
+        k = (int)kk;
+      }
+      so.starts[b] = make_int2(tau, k);
+    }
   }
   if (threadIdx.x == 0) {
     *num_active_out = run;
@@ -280,194 +346,292 @@ constexpr int LDT = LDW * 32;
 constexpr int RPT = MBM * 8 / LDT;     // tile rows handled per loader thread (8 sixteen-byte chunks a row)
 
 // =============================================================================
-// shrink_kernel: CTA (tile, slice i) computes h[t, i*R + j] = x[t] . a[slot][i*R + j]
-// for j < rank.  A cluster of `cl` CTAs splits the contraction (decode tiles are
-// few) and sums the partial h in cluster-rank order through distributed shared
-// memory.  Four consumer warps own 16 rows each; two loader warps gather the
-// tile's x rows (one TMA box when the tile is dense) and the slice's a rows
-// with 16-byte cp.async copies.
+// shrink_kernel: h[t, i*R + j] = x[t] . a[slot][i*R + j] for every slice i and
+// j < rank, over the slot-sorted tiles of at most 64 tokens.  The work, tiles x
+// stages of 64 columns of `in`, is split over G persistent CTAs by cost (the
+// grouping kernel writes each CTA's first (tile, stage)), so every CTA streams
+// about the same number of bytes whatever the ranks.  A stage holds 64 columns
+// of the tile's x rows (one TMA box when the tile's tokens are consecutive rows,
+// else 64 rows gathered with 16-byte cp.async) and of the first rank16 rows of
+// every slice of a[slot] (TMA boxes of 16 rows), all with the 128-byte swizzle,
+// so x is read once per tile for all slices; the ring runs on across tiles.  A
+// tile wholly inside one CTA's share is written to h directly; a tile shared by
+// several CTAs leaves fp32 partial sums in the workspace, and the CTA that
+// completes its stages (atomic ticket) adds them in the owners' order, so the
+// result does not depend on timing.  Eight consumer warps: two 32-row halves
+// times four quarters of the n * rank16 columns (at most QB 16-column blocks
+// each).  Two loader warps.
 // =============================================================================
-constexpr int SH_CWN = 4;   // shrink consumer warps
+constexpr int SH_CWN = 8;            // shrink consumer warps
+constexpr int SH_XB = MBM * KW * 2;  // x bytes of one stage (8 KB)
+constexpr int SH_BARS = 1024;        // barrier block in front of the ring
+constexpr int SH_MAX_CTAS = 320;     // bound on the persistent grid (partial-sum workspace)
 
-template <int RP>
+template <int QB>
 struct ShCfg {
-  static constexpr int STAGE = ((MBM + RP) * XP + 1023) / 1024 * 1024;   // x rows + a rows of one slice
-  static constexpr int NS = (54 * 1024) / STAGE < 2 ? 2 : (54 * 1024) / STAGE > 6 ? 6 : (54 * 1024) / STAGE;
-  static constexpr int BYTES = 1024 + NS * STAGE + 8 * (2 * NS + 2) + 64;
   static constexpr int THREADS = (SH_CWN + LDW) * 32;
-  static_assert(MBM * RP * 4 <= NS * STAGE, "the h exchange must fit in the stage ring");
+  static constexpr int CTAS = QB >= 4 ? 1 : 2;                  // per SM (register bound)
+  static constexpr int RING = CTAS == 1 ? 200 * 1024 : 100 * 1024;
+  static constexpr int BYTES = 1024 + SH_BARS + RING;
 };
 
-template <int RP>
-__global__ void __launch_bounds__(ShCfg<RP>::THREADS, RP >= 128 ? 2 : 4)
-    shrink_kernel(const __grid_constant__ CUtensorMap tmX, MArgs p) {
-  using C = ShCfg<RP>;
-  constexpr int NS = C::NS;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = align1024(smem_raw);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * C::STAGE);
-  uint64_t *empty = full + NS;
-  uint64_t *hready = empty + NS, *hdone = hready + 1;
-  float *hbuf = reinterpret_cast<float *>(smem);   // the exchange reuses the ring once the loads are over
+__device__ __forceinline__ bool before(int2 u, int2 v) { return u.x < v.x || (u.x == v.x && u.y < v.y); }
 
+template <int QB>
+__global__ void __launch_bounds__(ShCfg<QB>::THREADS, ShCfg<QB>::CTAS)
+    shrink_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA16,
+                  const __grid_constant__ CUtensorMap tmA32, const __grid_constant__ CUtensorMap tmA64, MArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = align1024(smem_raw);
+  uint64_t *full = reinterpret_cast<uint64_t *>(base);
+  uint64_t *empty = full + 16;
+  uint64_t *pdone = empty + 16, *pflag = pdone + 1;   // hand-off of a shared tile's partial sums
+  volatile int *last_flag = reinterpret_cast<volatile int *>(pflag + 1);
+  uint8_t *ring = base + SH_BARS;
+  const int NS = p.sh_ns, STAGE = p.sh_stage, nk = p.nk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cl = p.cl;
-  const int item = blockIdx.x / cl;
-  const int tile = item / p.n, i = item % p.n;
-  pdl_wait();
-  if (tile >= p.header[1]) return;   // the whole cluster: beyond the device-side tile count
-  const uint32_t crank = cl > 1 ? cluster_ctarank() : 0u;
-  const int4 td = p.tiles[tile];
-  const int slot = td.x, start = td.y, len = td.z;
-  const int rank = p.ranks[slot];
-  const bool dense = (LORA_MULTI_TMA & 1) && p.tma_ok && dense_tile(p.perm, start, len);
-  const int nk = (int)((p.in + KW - 1) / KW);
-  const int k_beg = (int)((int64_t)nk * crank / cl), k_end = (int)((int64_t)nk * (crank + 1) / cl);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], LDT + 1);
       mbar_init(&empty[s], SH_CWN);
     }
-    mbar_init(hready, cl > 1 ? SH_CWN * 32 * (cl - 1) : 1);
-    mbar_init(hdone, cl > 1 ? SH_CWN * 32 * (cl - 1) : 1);
+    mbar_init(pdone, SH_CWN);
+    mbar_init(pflag, 1);
     fence_barrier_init();
   }
-  if (cl > 1) cluster_sync_all(); else __syncthreads();
+  __syncthreads();
+  pdl_wait();
+  const int2 s0 = p.starts[blockIdx.x], s1 = p.starts[blockIdx.x + 1];
+  if (!before(s0, s1)) return;                        // no work (the whole CTA)
+  const int tlast = s1.y > 0 ? s1.x : s1.x - 1;      // last tile with a stage of this CTA
 
   if (warp >= SH_CWN) {
     // ---------------------------------------------------------------- loaders (64 threads)
     const int lt = threadIdx.x - SH_CWN * 32;
     const int ch = lt & 7;                         // 16-byte chunk of a row
-    const int t0 = p.perm[start];
-    if (lt == 0 && dense) prefetch_tmap(&tmX);
-    const __nv_bfloat16 *xrow[RPT];
-#pragma unroll
-    for (int k = 0; k < RPT; ++k) {
-      const int r = (lt >> 3) + k * (LDT / 8);
-      xrow[k] = r < len ? p.x + (int64_t)p.perm[start + r] * p.ldx : p.x;
-    }
-    const __nv_bfloat16 *as = p.a + (int64_t)slot * p.sa_slot + (int64_t)i * p.R * p.sa_row;
-    for (int g = 0; g < k_end - k_beg; ++g) {
-      const int s = g % NS;
-      if (g >= NS && !mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) break;
-      uint8_t *st = smem + s * C::STAGE;
-      const int64_t k0 = (int64_t)(k_beg + g) * KW;
-      const int64_t krem = p.in - k0 < (int64_t)KW ? p.in - k0 : (int64_t)KW;
-      const uint32_t nb = clamp16((int)krem * 2 - ch * 16);
-      if (dense) {
-        if (lt == 0) {
-          mbar_arrive_expect_tx(&full[s], MBM * KW * 2);
-          tma_load_2d(st, &tmX, &full[s], (int)k0, t0);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < RPT; ++k) {
-          const int r = (lt >> 3) + k * (LDT / 8);
-          cp_async16(st + r * XP + ch * 16, xrow[k] + k0 + ch * 8, r < len ? nb : 0u);
-        }
-        if (lt == 0) mbar_arrive(&full[s]);
+    if (lt == 0) {
+      if (p.tma_ok) prefetch_tmap(&tmX);
+      if (p.tma_a) {
+        prefetch_tmap(&tmA16);
+        prefetch_tmap(&tmA32);
+        prefetch_tmap(&tmA64);
       }
-      for (int j = lt >> 3; j < rank; j += LDT / 8)
-        cp_async16(st + (MBM + j) * XP + ch * 16, as + (int64_t)j * p.sa_row + k0 + ch * 8, nb);
-      cp_async_arrive(&full[s]);
+    }
+    int g = 0;
+    bool ok = true;
+    for (int tau = s0.x; tau <= tlast && ok; ++tau) {
+      const int kb = tau == s0.x ? s0.y : 0, ke = tau == s1.x ? s1.y : nk;
+      const int4 td = p.tiles[tau];
+      const int slot = td.x, start = td.y, len = td.z;
+      const int rank = p.ranks[slot];
+      const int r16 = (rank + 15) & ~15, ncols = p.n * r16;
+      const int t0 = p.perm[start];
+      // consecutive rows: one box (rows past len belong to other tokens and are never written)
+      const bool dense = (LORA_MULTI_TMA & 1) && p.tma_ok && p.perm[start + len - 1] - t0 == len - 1;
+      const __nv_bfloat16 *as = p.a + (int64_t)slot * p.sa_slot;
+      const uint32_t tx = (dense ? SH_XB : 0u) + (p.tma_a ? (uint32_t)ncols * KW * 2 : 0u);
+      // A thread keeps one tensor copy in flight at a time, so the copies of a
+      // stage are spread over the lanes of the first loader warp: lane 0 the x
+      // box, lane b the b-th adapter box (each slice's rank16 rows as boxes of
+      // 64, 32 and 16 rows; at most 3 per slice).
+      // gathered rows: this thread's 8 row addresses, loaded once per tile
+      const __nv_bfloat16 *xrow[RPT];
+#pragma unroll
+      for (int q = 0; q < RPT; ++q) {
+        const int r = (lt >> 3) + q * (LDT / 8);
+        xrow[q] = p.x + (!dense && r < len ? (int64_t)p.perm[start + r] * p.ldx : 0);
+      }
+      const CUtensorMap *bmap = nullptr;
+      int bdst = 0, brow = 0;
+      if (p.tma_a && lt >= 1 && lt < 32) {
+        int b = 0;
+        for (int i = 0; i < p.n && !bmap; ++i)
+          for (int j0 = 0; j0 < r16;) {
+            const int hb = r16 - j0 >= 64 ? 64 : r16 - j0 >= 32 ? 32 : 16;
+            if (++b == lt) {
+              bmap = hb == 64 ? &tmA64 : hb == 32 ? &tmA32 : &tmA16;
+              bdst = (i * r16 + j0) * 128;
+              brow = i * p.R + j0;
+              break;
+            }
+            j0 += hb;
+          }
+      }
+      for (int k = kb; k < ke; ++k, ++g) {
+        const int s = g % NS;
+        if (g >= NS && !wait_all(&empty[s], ((g / NS) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        uint8_t *st = ring + s * STAGE;
+        uint8_t *sa = st + SH_XB;
+        const int k0 = k * KW;
+        const int64_t krem = p.in - k0 < (int64_t)KW ? p.in - k0 : (int64_t)KW;
+        const uint32_t nb = clamp16((int)krem * 2 - ch * 16);
+        if (lt == 0) {
+          if (tx) mbar_arrive_expect_tx(&full[s], tx);
+          else mbar_arrive(&full[s]);
+        }
+        __syncwarp();
+        if (lt == 0 && dense) tma_load_2d(st, &tmX, &full[s], k0, t0);
+        if (bmap) tma_load_3d(sa + bdst, bmap, &full[s], k0, brow, slot);
+        if (!dense) {
+#pragma unroll
+          for (int q = 0; q < RPT; ++q) {
+            const int r = (lt >> 3) + q * (LDT / 8);
+            cp_async16(st + swz(r, ch * 16, 128), xrow[q] + k0 + ch * 8, r < len ? nb : 0u);
+          }
+        }
+        if (!p.tma_a) {
+          // rows j >= rank of a slice (padding, any value) are loaded too: their columns are dropped
+          for (int c = lt >> 3; c < ncols; c += LDT / 8) {
+            const int i = c / r16, j = c - i * r16;
+            const bool in_r = i * p.R + j < p.n * p.R;
+            cp_async16(sa + swz(c, ch * 16, 128), as + (int64_t)(in_r ? i * p.R + j : 0) * p.sa_row + k0 + ch * 8,
+                       in_r ? nb : 0u);
+          }
+        }
+        cp_async_arrive(&full[s]);
+      }
     }
     pdl_launch_dependents();
     return;
   }
 
   // ------------------------------------------------------------------ consumers
-  const int w = warp, gq = lane >> 2, cq = lane & 3;
-  const bool live = 16 * w < len;
-  float hacc[RP / 8][4];
-#pragma unroll
-  for (int t = 0; t < RP / 8; ++t) hacc[t][0] = hacc[t][1] = hacc[t][2] = hacc[t][3] = 0.f;
+  const int w = warp, rh = w & 1, cqt = w >> 1;   // 32-row half, column quarter
+  const int gq = lane >> 2, cq = lane & 3, l = lane;
+  int g = 0, nshared = 0;
   bool ok = true;
-  const int l = lane_id();
-  for (int g = 0; g < k_end - k_beg; ++g) {
-    const int s = g % NS;
-    if (!(ok = wait_all(&full[s], (g / NS) & 1))) break;
-    const uint32_t xb = smem_u32(smem + s * C::STAGE), ab = xb + MBM * XP;
-    const int64_t k0 = (int64_t)(k_beg + g) * KW;
-    if (live) {
+  for (int tau = s0.x; tau <= tlast && ok; ++tau) {
+    const int kb = tau == s0.x ? s0.y : 0, ke = tau == s1.x ? s1.y : nk;
+    const int4 td = p.tiles[tau];
+    const int slot = td.x, start = td.y, len = td.z;
+    const int rank = p.ranks[slot];
+    const int r16 = (rank + 15) & ~15;
+    const int nbt = p.n * r16 / 16;                 // 16-column blocks of this slot
+    const int nbq = (nbt + 3) / 4;                  // <= QB
+    const int cb0 = cqt * nbq, cb1 = min(nbt, cb0 + nbq);
+    const bool live = 32 * rh < len && cb0 < cb1;
+    float hacc[2][2 * QB][4];
 #pragma unroll
-      for (int kk = 0; kk < KW / 16; ++kk) {
-        if (k0 + kk * 16 >= p.in) break;
-        uint32_t a[4];
-        const int ar = 16 * w + (l & 15), ac = kk * 16 + ((l >> 4) << 3);
-        ldsm_x4(xb + (dense ? swz_off(ar, ac) : (uint32_t)(ar * XP + ac * 2)), a[0], a[1], a[2], a[3]);
+    for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int np = 0; np < RP / 16; ++np) {
-          if (np * 16 >= rank) break;
-          uint32_t b[4];
-          ldb_p(ab, XP, np * 16, kk * 16, b);
-          mma_bf16(hacc[2 * np], a, b[0], b[1]);
-          mma_bf16(hacc[2 * np + 1], a, b[2], b[3]);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-  }
-  // columns past the slot's rank come from unloaded (stale) rows of a: zero them
+      for (int t = 0; t < 2 * QB; ++t) hacc[m][t][0] = hacc[m][t][1] = hacc[m][t][2] = hacc[m][t][3] = 0.f;
+    for (int k = kb; k < ke; ++k, ++g) {
+      const int s = g % NS;
+      if (!(ok = wait_all(&full[s], (g / NS) & 1))) break;
+      const uint32_t xb = smem_u32(ring + s * STAGE), ab = xb + SH_XB;
+      const int k0 = k * KW;
+      if (live) {
 #pragma unroll
-  for (int nt = 0; nt < RP / 8; ++nt) {
-    const int j = nt * 8 + 2 * cq;
-    if (j >= rank) hacc[nt][0] = hacc[nt][2] = 0.f;
-    if (j + 1 >= rank) hacc[nt][1] = hacc[nt][3] = 0.f;
-  }
-  const int r0 = 16 * w + gq;
-  if (cl > 1) {
-    named_bar_sync(1, SH_CWN * 32);   // every consumer warp is done with the ring
+        for (int kk = 0; kk < KW / 16; ++kk) {
+          if (k0 + kk * 16 >= p.in) break;
+          uint32_t a[2][4];
 #pragma unroll
-    for (int nt = 0; nt < RP / 8; ++nt) {
-      *reinterpret_cast<float2 *>(&hbuf[r0 * RP + nt * 8 + 2 * cq]) = make_float2(hacc[nt][0], hacc[nt][1]);
-      *reinterpret_cast<float2 *>(&hbuf[(r0 + 8) * RP + nt * 8 + 2 * cq]) = make_float2(hacc[nt][2], hacc[nt][3]);
-    }
-    for (int q = 0; q < cl; ++q)
-      if (q != (int)crank) mbar_arrive_remote(hready, q);
-    if (!wait_all<true>(hready, 0)) ok = false;
-    if (ok && live && (w % cl) == (int)crank) {
+          for (int m = 0; m < 2; ++m)
+            ldsm_x4(xb + swz(32 * rh + 16 * m + (l & 15), (kk * 16 + ((l >> 4) << 3)) * 2, 128), a[m][0], a[m][1],
+                    a[m][2], a[m][3]);
 #pragma unroll
-      for (int nt = 0; nt < RP / 8; ++nt) {
-        float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
-        for (int q = 0; q < cl; ++q) {
-          float2 v0, v1;
-          if (q == (int)crank) {
-            v0 = make_float2(hacc[nt][0], hacc[nt][1]);
-            v1 = make_float2(hacc[nt][2], hacc[nt][3]);
-          } else {
-            v0 = ld_dsmem_f2(&hbuf[r0 * RP + nt * 8 + 2 * cq], q);
-            v1 = ld_dsmem_f2(&hbuf[(r0 + 8) * RP + nt * 8 + 2 * cq], q);
+          for (int q = 0; q < QB; ++q) {
+            if (cb0 + q >= cb1) break;
+            uint32_t b[4];
+            ldsm_x4(ab + swz((cb0 + q) * 16 + (l & 7) + ((l >> 4) << 3), (kk * 16 + (((l >> 3) & 1) << 3)) * 2, 128),
+                    b[0], b[1], b[2], b[3]);
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              mma_bf16(hacc[m][2 * q], a[m], b[0], b[1]);
+              mma_bf16(hacc[m][2 * q + 1], a[m], b[2], b[3]);
+            }
           }
-          s0.x += v0.x; s0.y += v0.y; s1.x += v1.x; s1.y += v1.y;
         }
-        hacc[nt][0] = s0.x; hacc[nt][1] = s0.y; hacc[nt][2] = s1.x; hacc[nt][3] = s1.y;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (!ok) break;
+    const bool whole = kb == 0 && ke == nk;
+    bool write = whole;
+    if (!whole) {
+      // a share of the tile: fp32 partial sums to this CTA's slot (0: its first tile, 1: its last)
+      float *part = p.part + (size_t)(2 * blockIdx.x + (tau == s0.x ? 0 : 1)) * MBM * p.sh_nc;
+      if (live) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int t = 0; t < 2 * QB; ++t) {
+            if (t >= 2 * (cb1 - cb0)) break;
+            const int r = 32 * rh + 16 * m + gq, c = cb0 * 16 + t * 8 + 2 * cq;
+            *reinterpret_cast<float2 *>(&part[r * p.sh_nc + c]) = make_float2(hacc[m][t][0], hacc[m][t][1]);
+            *reinterpret_cast<float2 *>(&part[(r + 8) * p.sh_nc + c]) = make_float2(hacc[m][t][2], hacc[m][t][3]);
+          }
+      }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pdone);
+      const uint32_t ph = nshared++ & 1;
+      if (threadIdx.x == 0) {
+        int last = 0;
+        if (mbar_wait(pdone, ph)) {
+          last = atomicAdd(&p.tickets[tau], ke - kb) + (ke - kb) == nk;
+          __threadfence();
+        }
+        *last_flag = last;
+        mbar_arrive(pflag);
+      }
+      if (!(ok = wait_all(pflag, ph))) break;
+      write = *last_flag != 0;
+      if (write && live) {
+        // the owners of the tile are consecutive CTAs: add their partials in order
+        int bf = blockIdx.x;
+        while (bf > 0 && before(make_int2(tau, 0), p.starts[bf])) --bf;
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int t = 0; t < 2 * QB; ++t) hacc[m][t][0] = hacc[m][t][1] = hacc[m][t][2] = hacc[m][t][3] = 0.f;
+        for (int b = bf;; ++b) {
+          const int2 sb = p.starts[b];
+          if (b > bf && sb.x != tau) break;                 // past the tile's last owner
+          if (!before(sb, p.starts[b + 1])) continue;       // an empty share
+          const float *pb = p.part + (size_t)(2 * b + (sb.x == tau ? 0 : 1)) * MBM * p.sh_nc;
+#pragma unroll
+          for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int t = 0; t < 2 * QB; ++t) {
+              if (t >= 2 * (cb1 - cb0)) break;
+              const int r = 32 * rh + 16 * m + gq, c = cb0 * 16 + t * 8 + 2 * cq;
+              const float2 v0 = __ldcg(reinterpret_cast<const float2 *>(&pb[r * p.sh_nc + c]));
+              const float2 v1 = __ldcg(reinterpret_cast<const float2 *>(&pb[(r + 8) * p.sh_nc + c]));
+              hacc[m][t][0] += v0.x; hacc[m][t][1] += v0.y; hacc[m][t][2] += v1.x; hacc[m][t][3] += v1.y;
+            }
+        }
       }
     }
-    for (int q = 0; q < cl; ++q)
-      if (q != (int)crank) mbar_arrive_remote(hdone, q);
-  }
-  // h rows < len, columns j < rank of slice i; cluster CTA q writes the warps w % cl == q
-  if (ok && live && (w % cl) == (int)crank) {
+    // h rows < len, columns j < rank of each slice (columns past the rank come from padding rows of a)
+    if (write && live) {
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int r = r0 + 8 * hf;
-      if (r >= len) continue;
-      float *hrow = p.h + (int64_t)p.perm[start + r] * p.ldh + (int64_t)i * p.R;
+      for (int m = 0; m < 2; ++m)
 #pragma unroll
-      for (int nt = 0; nt < RP / 8; ++nt) {
-        const int j = nt * 8 + 2 * cq;
-        if (j + 1 < rank) {
-          *reinterpret_cast<float2 *>(&hrow[j]) = make_float2(hacc[nt][2 * hf], hacc[nt][2 * hf + 1]);
-        } else if (j < rank) {
-          hrow[j] = hacc[nt][2 * hf];
+        for (int hf = 0; hf < 2; ++hf) {
+          const int r = 32 * rh + 16 * m + gq + 8 * hf;
+          if (r >= len) continue;
+          float *hrow = p.h + (int64_t)p.perm[start + r] * p.ldh;
+#pragma unroll
+          for (int t = 0; t < 2 * QB; ++t) {
+            if (t >= 2 * (cb1 - cb0)) break;
+            const int c = cb0 * 16 + t * 8 + 2 * cq, i = c / r16, j = c - i * r16;
+            float *hp2 = hrow + (int64_t)i * p.R + j;
+            if (j + 1 < rank) {
+              *reinterpret_cast<float2 *>(hp2) = make_float2(hacc[m][t][2 * hf], hacc[m][t][2 * hf + 1]);
+            } else if (j < rank) {
+              hp2[0] = hacc[m][t][2 * hf];
+            }
+          }
         }
-      }
     }
   }
   pdl_launch_dependents();
-  if (cl > 1) wait_all<true>(hdone, 0);   // peers are done reading this CTA's ring
 }
 
 // =============================================================================
@@ -768,6 +932,24 @@ size_t sched_bytes(int64_t T, int S) {
 // h of apply_linear, kept between its two kernels (n * R <= kMaxHC columns)
 size_t hbuf_bytes(int64_t T, int R) { return ws_round((size_t)T * std::min(kMaxHC, LORA_MAX_SLICES * R) * 4); }
 
+// The shrink's split of work: CTA starts, per-tile tickets, partial sums of shared tiles.
+struct ShrinkWs {
+  int2 *starts;
+  int *tickets;
+  float *part;
+};
+int shrink_nc_bound(int R) { return (int)std::min<int64_t>(kMaxHC, (int64_t)LORA_MAX_SLICES * round_up(R, 16)); }
+size_t shrink_ws_bytes(int64_t T, int S, int R) {
+  return ws_round((size_t)(SH_MAX_CTAS + 1) * 8) + ws_round((size_t)max_tiles(T, S) * 4) +
+         ws_round((size_t)2 * SH_MAX_CTAS * MBM * shrink_nc_bound(R) * 4);
+}
+bool carve_shrink(WsCarver &c, int64_t T, int S, int R, ShrinkWs &sw) {
+  sw.starts = (int2 *)c.take((size_t)(SH_MAX_CTAS + 1) * 8);
+  sw.tickets = (int *)c.take((size_t)max_tiles(T, S) * 4);
+  sw.part = (float *)c.take((size_t)2 * SH_MAX_CTAS * MBM * shrink_nc_bound(R) * 4);
+  return sw.starts && sw.tickets && sw.part;
+}
+
 bool carve_sched(WsCarver &c, int64_t T, int S, SchedPtrs &sp) {
   sp.header = (int *)c.take(256);
   sp.counts = (int *)c.take((size_t)S * 4);
@@ -777,14 +959,15 @@ bool carve_sched(WsCarver &c, int64_t T, int S, SchedPtrs &sp) {
 }
 
 lora_status_t launch_group(const lora_addressing_t &ad, const int32_t *ranks, int32_t *counts, int32_t *perm,
-                           int32_t *num_active, int *header, int4 *tiles, cudaStream_t st) {
+                           int32_t *num_active, int *header, int4 *tiles, cudaStream_t st,
+                           SplitOut so = SplitOut{nullptr, nullptr, 0, 0, 0, 0}) {
   const int S = ad.num_slots;
-  int nw = (int)std::max<int64_t>(1, (160 * 1024 / 4 - 256 - S) / S);   // shared-memory bound
+  int nw = (int)std::max<int64_t>(1, (160 * 1024 / 4 - 256 - 3 * S) / S);   // shared-memory bound
   nw = std::min<int64_t>({nw, 32, std::max<int64_t>(1, ceil_div(ad.num_tokens, LORA_GROUP_TOKENS_PER_WARP))});
-  const size_t smem = (size_t)(nw * S + S + 160) * 4;
+  const size_t smem = (size_t)(nw * S + 3 * S + 161) * 4;
   LORA_CUDA(ensure_smem((const void *)group_kernel, smem));
   LORA_CUDA(launch(group_kernel, dim3(1), dim3(nw * 32), smem, st, 1, true, ad.slots, ad.num_tokens, S,
-                   ad.max_rank, ranks, counts, perm, num_active, header, tiles, (int)MBM));
+                   ad.max_rank, ranks, counts, perm, num_active, header, tiles, (int)MBM, so));
   return LORA_OK;
 }
 
@@ -796,29 +979,61 @@ bool map_rows(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int6
   return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int RP>
-lora_status_t launch_shrink(MArgs a, int64_t T, cudaStream_t st) {
-  auto kern = shrink_kernel<RP>;
-  const size_t smem = ShCfg<RP>::BYTES;
+// Boxes of `box_rows` rows x 64 columns of the adapter stack a[S][rows][cols] (128-byte swizzle).
+bool map_adapter(CUtensorMap *m, const void *base, int64_t S, int64_t rows, int64_t cols, int64_t s_slot,
+                 int64_t s_row, uint32_t box_rows) {
+  uint64_t dims[3] = {(uint64_t)cols, (uint64_t)rows, (uint64_t)S};
+  uint64_t str[2] = {(uint64_t)s_row * 2, (uint64_t)s_slot * 2};
+  uint32_t box[3] = {64, box_rows, 1};
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// 16-column blocks per consumer quarter of the shrink for the widest slot.
+int shrink_qb(int n, int R) { return (int)std::min<int64_t>(4, ceil_div((int64_t)n * round_up(R, 16) / 16, 4)); }
+
+template <int QB>
+int shrink_grid() {
+  const int occ = occupancy((const void *)shrink_kernel<QB>, ShCfg<QB>::THREADS, ShCfg<QB>::BYTES);
+  return (int)std::min<int64_t>(SH_MAX_CTAS, std::max<int64_t>(1, (int64_t)occ * num_sms()));
+}
+int shrink_grid(int n, int R) {
+  switch (shrink_qb(n, R)) {
+    case 1: return shrink_grid<1>();
+    case 2: return shrink_grid<2>();
+    case 3: return shrink_grid<3>();
+    default: return shrink_grid<4>();
+  }
+}
+
+template <int QB>
+lora_status_t launch_shrink(MArgs a, int64_t T, int G, cudaStream_t st) {
+  auto kern = shrink_kernel<QB>;
+  const size_t smem = ShCfg<QB>::BYTES;
   LORA_CUDA(ensure_smem((const void *)kern, smem));
-  CUtensorMap tmX;
+  CUtensorMap tmX, tmA16, tmA32, tmA64;
   a.tma_ok = map_rows(&tmX, a.x, T, a.in, a.ldx) ? 1 : 0;
-  const int occ = occupancy((const void *)kern, ShCfg<RP>::THREADS, smem);
-  const int64_t items = (int64_t)max_tiles(T, a.S) * a.n, cap = (int64_t)occ * num_sms();
-  int cl = 1;
-  while (cl * 2 <= 8 && items * cl * 2 <= cap) cl *= 2;
-  while (cl > 1 && ceil_div(a.in, KW) < cl) cl /= 2;
-  a.cl = cl;
-  LORA_CUDA(launch(kern, dim3((unsigned)(items * cl)), dim3(ShCfg<RP>::THREADS), smem, st, cl, true, tmX, a));
+  const int64_t arows = (int64_t)a.n * a.R;
+  a.tma_a = map_adapter(&tmA16, a.a, a.S, arows, a.in, a.sa_slot, a.sa_row, 16) &&
+                    map_adapter(&tmA32, a.a, a.S, arows, a.in, a.sa_slot, a.sa_row, 32) &&
+                    map_adapter(&tmA64, a.a, a.S, arows, a.in, a.sa_slot, a.sa_row, 64)
+                ? 1
+                : 0;
+  const int nc = a.n * (int)round_up(a.R, 16);   // most columns a slot can have
+  a.sh_nc = nc;
+  a.sh_stage = SH_XB + nc * KW * 2;
+  a.sh_ns = std::min(16, ShCfg<QB>::RING / a.sh_stage);
+  if (a.sh_ns < 2 || nc > shrink_nc_bound(a.R)) return LORA_ERR_UNSUPPORTED;
+  LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(ShCfg<QB>::THREADS), smem, st, 1, true, tmX, tmA16, tmA32, tmA64,
+                   a));
   return LORA_OK;
 }
 
-lora_status_t dispatch_shrink(const MArgs &a, int64_t T, cudaStream_t st) {
-  switch (rank_bucket(a.R)) {
-    case 16: return launch_shrink<16>(a, T, st);
-    case 32: return launch_shrink<32>(a, T, st);
-    case 64: return launch_shrink<64>(a, T, st);
-    default: return launch_shrink<128>(a, T, st);
+lora_status_t dispatch_shrink(const MArgs &a, int64_t T, int G, cudaStream_t st) {
+  switch (shrink_qb(a.n, a.R)) {
+    case 1: return launch_shrink<1>(a, T, G, st);
+    case 2: return launch_shrink<2>(a, T, G, st);
+    case 3: return launch_shrink<3>(a, T, G, st);
+    default: return launch_shrink<4>(a, T, G, st);
   }
 }
 
@@ -900,9 +1115,33 @@ MArgs margs(const MultiArgs &m, const SchedPtrs &sp) {
   return a;
 }
 
-lora_status_t schedule(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, cudaStream_t st) {
+lora_status_t schedule(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, cudaStream_t st,
+                       SplitOut so = SplitOut{nullptr, nullptr, 0, 0, 0, 0}) {
   if (!carve_sched(c, m.addr.num_tokens, m.addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
-  return launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st);
+  return launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st, so);
+}
+
+// Schedule plus the shrink's work split, then the shrink itself (h written to a.h).
+lora_status_t schedule_and_shrink(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, MArgs *out, float *h,
+                                  int64_t ldh, cudaStream_t st) {
+  const int64_t T = m.addr.num_tokens;
+  const int S = m.addr.num_slots, R = m.addr.max_rank;
+  if (!carve_sched(c, T, S, sp)) return LORA_ERR_WORKSPACE;
+  ShrinkWs sw;
+  if (!carve_shrink(c, T, S, R, sw)) return LORA_ERR_WORKSPACE;
+  const int G = shrink_grid(m.n, R);
+  const int nk = (int)std::max<int64_t>(1, ceil_div(m.in, KW));
+  SplitOut so{sw.starts, sw.tickets, G, m.n, nk, max_tiles(T, S)};
+  LORA_TRY(launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st, so));
+  MArgs a = margs(m, sp);
+  a.h = h;
+  a.ldh = ldh;
+  a.starts = sw.starts;
+  a.tickets = sw.tickets;
+  a.part = sw.part;
+  a.nk = nk;
+  *out = a;
+  return dispatch_shrink(a, T, G, st);
 }
 
 }  // namespace
@@ -911,8 +1150,9 @@ size_t multi_ws_bytes(int op, int64_t T, int64_t in, int64_t O, int R, int S) {
   (void)in;
   (void)O;
   if (T <= 0) return 0;
-  if (op == LORA_OP_GROUP_BY_SLOT || op == LORA_OP_SHRINK || op == LORA_OP_EXPAND) return sched_bytes(T, S);
-  if (op == LORA_OP_APPLY_LINEAR) return sched_bytes(T, S) + hbuf_bytes(T, R);
+  if (op == LORA_OP_GROUP_BY_SLOT || op == LORA_OP_EXPAND) return sched_bytes(T, S);
+  if (op == LORA_OP_SHRINK) return sched_bytes(T, S) + shrink_ws_bytes(T, S, R);
+  if (op == LORA_OP_APPLY_LINEAR) return sched_bytes(T, S) + hbuf_bytes(T, R) + shrink_ws_bytes(T, S, R);
   return 0;
 }
 
@@ -934,8 +1174,8 @@ lora_status_t shrink(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t st) {
   LORA_TRY(check_seg(m, true, false));
   WsCarver c(ws, ws_bytes);
   SchedPtrs sp;
-  LORA_TRY(schedule(m, c, sp, st));
-  return dispatch_shrink(margs(m, sp), m.addr.num_tokens, st);
+  MArgs a;
+  return schedule_and_shrink(m, c, sp, &a, m.h, m.ldh, st);
 }
 
 lora_status_t expand(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t st) {
@@ -949,14 +1189,11 @@ lora_status_t expand(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t st) {
 lora_status_t apply_linear(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t st) {
   LORA_TRY(check_seg(m, true, true));
   WsCarver c(ws, ws_bytes);
-  SchedPtrs sp;
-  LORA_TRY(schedule(m, c, sp, st));
   float *h = (float *)c.take(hbuf_bytes(m.addr.num_tokens, m.addr.max_rank));
   if (!h) return LORA_ERR_WORKSPACE;
-  MArgs a = margs(m, sp);
-  a.h = h;
-  a.ldh = (int64_t)m.n * m.addr.max_rank;
-  LORA_TRY(dispatch_shrink(a, m.addr.num_tokens, st));
+  SchedPtrs sp;
+  MArgs a;
+  LORA_TRY(schedule_and_shrink(m, c, sp, &a, h, (int64_t)m.n * m.addr.max_rank, st));
   return dispatch_expand(a, m.addr.num_tokens, st);
 }
 
