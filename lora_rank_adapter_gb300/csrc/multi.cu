@@ -23,6 +23,7 @@
 // Adapter padding (rows / columns past a slot's rank, which may hold anything)
 // is masked in registers, never trusted.
 #include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
 #include "host_common.h"
@@ -58,6 +59,10 @@ struct MArgs {
   int tma_a;                      // the tensor map of a is valid (shrink)
   int sh_ns, sh_stage;            // shrink: stages in the ring, bytes per stage
   int sh_nc, nk;                  // shrink: partial-sum row pitch (columns), stages per tile
+  int T;                          // number of tokens (rows of x)
+  int tc_cols;                    // shrink: tensor-memory columns of the accumulator
+  int a_one_slot;                 // shrink: the adapter map has one slot (slot stride 0)
+  int nsub;                       // expand: 64-row sub-tiles per tile
   const int2 *starts;             // shrink: first (tile, stage) of each CTA, [G + 1]
   int *tickets;                   // shrink: stages finished per tile
   float *part;                    // shrink: partial sums, [2 G][64][sh_nc]
@@ -182,13 +187,13 @@ __device__ __forceinline__ void block_scan2(int a, int b, int &ea, int &eb, int 
 constexpr int GU = 8;   // tokens per lane per batch in group_kernel
 
 // Optional output of the grouping for the shrink: the split of its work over G
-// persistent CTAs.  Tile tau costs nk stages of n * rank16(slot) + 64 rows of
+// persistent CTAs.  Tile tau costs nk stages of n * rank16(slot) + xw rows of
 // 128 bytes (a rows of every slice plus x rows); CTA b starts at the first
 // (tile, stage) whose cost offset is at least floor(total * b / G).
 struct SplitOut {
   int2 *starts;    // [G + 1] (tile, stage); starts[G] = (tiles, 0)
   int *tickets;    // [ntick] zeroed: stages of a tile finished so far
-  int G, n, nk, ntick;
+  int G, n, nk, ntick, xw;   // xw: x rows of a tile per stage
 };
 // Tokens per warp the grouping aims for (fewer warps: shorter scans and barriers).
 #ifndef LORA_GROUP_TOKENS_PER_WARP
@@ -262,7 +267,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
     run += tc;
     trun += tt;
     if (so.G > 0) {
-      const int cost = s < S ? nt * (so.n * ((srank[s] + 15) & ~15) + 64) : 0;
+      const int cost = s < S ? nt * (so.n * ((srank[s] + 15) & ~15) + so.xw) : 0;
       int ecost, dummy, tcost, tdummy;
       block_scan2(cost, 0, ecost, dummy, tcost, tdummy, sh);
       if (s < S) spc[s] = crun + ecost;
@@ -274,8 +279,13 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
     for (int i = threadIdx.x; i < so.ntick; i += blockDim.x) so.tickets[i] = 0;
     __syncthreads();
     const int64_t total = (int64_t)crun * so.nk;
+    // every share holds at least nk / 32 stages of the widest slot, so a tile has
+    // at most 33 owners; CTAs past the shares used get none
+    const int64_t wmax = (int64_t)so.n * ((R + 15) & ~15) + so.xw;
+    const int64_t min_share = (int64_t)((so.nk + 31) / 32) * wmax;
+    const int Gu = (int)max((int64_t)1, min((int64_t)so.G, total / min_share));
     for (int b = threadIdx.x; b <= so.G; b += blockDim.x) {
-      const int64_t c = total * b / so.G;
+      const int64_t c = b >= Gu ? total : total * b / Gu;
       int tau = trun, k = 0;
       if (c < total) {
         int lo = 0, hi = S - 1;   // the last slot whose cost starts at or before c
@@ -284,7 +294,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
           if ((int64_t)spc[mid] * so.nk <= c) lo = mid;
           else hi = mid - 1;
         }
-        const int64_t w = so.n * ((srank[lo] + 15) & ~15) + 64;
+        const int64_t w = so.n * ((srank[lo] + 15) & ~15) + so.xw;
         const int64_t o = c - (int64_t)spc[lo] * so.nk;
         int64_t ti = o / (so.nk * w);
         int64_t kk = (o - ti * so.nk * w + w - 1) / w;
@@ -347,75 +357,98 @@ constexpr int RPT = MBM * 8 / LDT;     // tile rows handled per loader thread (8
 
 // =============================================================================
 // shrink_kernel: h[t, i*R + j] = x[t] . a[slot][i*R + j] for every slice i and
-// j < rank, over the slot-sorted tiles of at most 64 tokens.  The work, tiles x
-// stages of 64 columns of `in`, is split over G persistent CTAs by cost (the
-// grouping kernel writes each CTA's first (tile, stage)), so every CTA streams
-// about the same number of bytes whatever the ranks.  A stage holds 64 columns
-// of the tile's x rows (one TMA box when the tile's tokens are consecutive rows,
-// else 64 rows gathered with 16-byte cp.async) and of the first rank16 rows of
-// every slice of a[slot] (TMA boxes of 16 rows), all with the 128-byte swizzle,
-// so x is read once per tile for all slices; the ring runs on across tiles.  A
-// tile wholly inside one CTA's share is written to h directly; a tile shared by
-// several CTAs leaves fp32 partial sums in the workspace, and the CTA that
-// completes its stages (atomic ticket) adds them in the owners' order, so the
-// result does not depend on timing.  Eight consumer warps: two 32-row halves
-// times four quarters of the n * rank16 columns (at most QB 16-column blocks
-// each).  Two loader warps.
+// j < rank, over the slot-sorted tiles of at most 128 tokens, on the
+// fifth-generation tensor cores.  The work, tiles x stages of 64 columns of
+// `in`, is split over persistent CTAs (one per SM) by cost: the grouping kernel
+// writes each CTA's first (tile, stage), so every CTA streams about the same
+// number of bytes whatever the ranks.  A warp keeps one tensor-copy instruction
+// in flight at a time (its lanes' copies run together), so the stages are dealt
+// round-robin to several loader warps: x loaders take the tile's 128 x rows (one
+// 128-row box when the tile's tokens are consecutive rows, else lane q gathers
+// rows 4q..4q+3 with one four-row gather copy), adapter loaders the first rank16
+// rows of every slice of a[slot] (lane b: the b-th box of 64, 32 or 16 rows),
+// all with the 128-byte swizzle, into a ring that runs on across tiles.  Lane 0
+// of the MMA warp issues four 128 x (n * rank16) x 16 MMAs per stage into a
+// tensor-memory accumulator (x read once per tile for all slices); warps 4-7
+// drain the accumulator, one token row per thread.  A tile wholly inside one CTA's share
+// is written to h directly; a tile shared by several CTAs leaves fp32 partial
+// sums in the workspace, and the CTA that completes its stages (atomic ticket)
+// adds them in the owners' order, so the result does not depend on timing.
 // =============================================================================
-constexpr int SH_CWN = 8;            // shrink consumer warps
-constexpr int SH_XB = MBM * KW * 2;  // x bytes of one stage (8 KB)
-constexpr int SH_BARS = 1024;        // barrier block in front of the ring
-constexpr int SH_MAX_CTAS = 320;     // bound on the persistent grid (partial-sum workspace)
-
-template <int QB>
-struct ShCfg {
-  static constexpr int THREADS = (SH_CWN + LDW) * 32;
-  static constexpr int CTAS = QB >= 4 ? 1 : 2;                  // per SM (register bound)
-  static constexpr int RING = CTAS == 1 ? 200 * 1024 : 100 * 1024;
-  static constexpr int BYTES = 1024 + SH_BARS + RING;
-};
+constexpr int TC_M = 128;                  // tokens per tile (accumulator rows)
+constexpr int TC_XB = TC_M * KW * 2;       // x bytes of one stage (16 KB)
+// Warp roles: x loaders [0, TC_XW), drain [4, 8), the MMA warp, adapter loaders
+// [TC_AW0, TC_AW0 + TC_AW).  Two CTAs an SM (smaller ring, fewer loader warps)
+// overlap one CTA's prologue, drains and final sums with the other's streaming.
+#ifndef LORA_SHRINK_2CTA
+#define LORA_SHRINK_2CTA 0
+#endif
+#if LORA_SHRINK_2CTA
+constexpr int TC_CTAS = 2, TC_THREADS = 256, TC_XW = 2, TC_MMA_WARP = 2, TC_AW0 = 3, TC_AW = 1;
+constexpr int TC_RING = 108 * 1024;
+#else
+constexpr int TC_CTAS = 1, TC_THREADS = 352, TC_XW = 4, TC_MMA_WARP = 8, TC_AW0 = 9, TC_AW = 2;
+constexpr int TC_RING = 200 * 1024;
+#endif
+constexpr int TC_MAX_OWNERS = 64;          // owners of a shared tile listed for the final sum
+constexpr int TC_BYTES = 1024 + 1024 + TC_RING;
+constexpr int SH_MAX_CTAS = 160;           // bound on the persistent grid (partial-sum workspace)
 
 __device__ __forceinline__ bool before(int2 u, int2 v) { return u.x < v.x || (u.x == v.x && u.y < v.y); }
 
-template <int QB>
-__global__ void __launch_bounds__(ShCfg<QB>::THREADS, ShCfg<QB>::CTAS)
-    shrink_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA16,
-                  const __grid_constant__ CUtensorMap tmA32, const __grid_constant__ CUtensorMap tmA64, MArgs p) {
+__global__ void __launch_bounds__(TC_THREADS, TC_CTAS)
+    shrink_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXd,
+                  const __grid_constant__ CUtensorMap tmA16, const __grid_constant__ CUtensorMap tmA32,
+                  const __grid_constant__ CUtensorMap tmA64, MArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = align1024(smem_raw);
   uint64_t *full = reinterpret_cast<uint64_t *>(base);
   uint64_t *empty = full + 16;
-  uint64_t *pdone = empty + 16, *pflag = pdone + 1;   // hand-off of a shared tile's partial sums
-  volatile int *last_flag = reinterpret_cast<volatile int *>(pflag + 1);
-  uint8_t *ring = base + SH_BARS;
+  uint64_t *accf = empty + 16, *acce = accf + 1;       // accumulator written / drained
+  uint64_t *pdone = acce + 1, *pflag = pdone + 1;      // hand-off of a shared tile's partial sums
+  uint64_t *mdone = pflag + 1;                         // every MMA of this CTA has completed
+  volatile int *last_flag = reinterpret_cast<volatile int *>(mdone + 1);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mdone + 2);
+  int *owners = reinterpret_cast<int *>(mdone + 3);   // [TC_MAX_OWNERS] partial slots of the owners, in order
+  uint8_t *ring = base + 1024;
   const int NS = p.sh_ns, STAGE = p.sh_stage, nk = p.nk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], LDT + 1);
-      mbar_init(&empty[s], SH_CWN);
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
     }
-    mbar_init(pdone, SH_CWN);
+    mbar_init(accf, 1);
+    mbar_init(acce, 4);
+    mbar_init(pdone, 4);
     mbar_init(pflag, 1);
+    mbar_init(mdone, 1);
     fence_barrier_init();
   }
+  if (warp == TC_MMA_WARP) tmem_alloc(tmem_slot, (uint32_t)p.tc_cols);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   pdl_wait();
   const int2 s0 = p.starts[blockIdx.x], s1 = p.starts[blockIdx.x + 1];
-  if (!before(s0, s1)) return;                        // no work (the whole CTA)
+  const bool any = before(s0, s1);
   const int tlast = s1.y > 0 ? s1.x : s1.x - 1;      // last tile with a stage of this CTA
+  const bool has_k = p.in > 0;
 
-  if (warp >= SH_CWN) {
-    // ---------------------------------------------------------------- loaders (64 threads)
-    const int lt = threadIdx.x - SH_CWN * 32;
-    const int ch = lt & 7;                         // 16-byte chunk of a row
-    if (lt == 0) {
-      if (p.tma_ok) prefetch_tmap(&tmX);
-      if (p.tma_a) {
+  const bool aw = warp >= TC_AW0 && warp < TC_AW0 + TC_AW;   // adapter loader
+  if (any && (warp < TC_XW || aw)) {
+    // ---------------------------------------------------------------- loader warps
+    const int par = aw ? warp - TC_AW0 : warp, nw = aw ? TC_AW : TC_XW;   // stages g % nw == par
+    if (lane == 0 && has_k) {
+      if (aw) {
         prefetch_tmap(&tmA16);
         prefetch_tmap(&tmA32);
         prefetch_tmap(&tmA64);
+      } else {
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmXd);
       }
     }
     int g = 0;
@@ -426,30 +459,28 @@ __global__ void __launch_bounds__(ShCfg<QB>::THREADS, ShCfg<QB>::CTAS)
       const int slot = td.x, start = td.y, len = td.z;
       const int rank = p.ranks[slot];
       const int r16 = (rank + 15) & ~15, ncols = p.n * r16;
-      const int t0 = p.perm[start];
-      // consecutive rows: one box (rows past len belong to other tokens and are never written)
-      const bool dense = (LORA_MULTI_TMA & 1) && p.tma_ok && p.perm[start + len - 1] - t0 == len - 1;
-      const __nv_bfloat16 *as = p.a + (int64_t)slot * p.sa_slot;
-      const uint32_t tx = (dense ? SH_XB : 0u) + (p.tma_a ? (uint32_t)ncols * KW * 2 : 0u);
-      // A thread keeps one tensor copy in flight at a time, so the copies of a
-      // stage are spread over the lanes of the first loader warp: lane 0 the x
-      // box, lane b the b-th adapter box (each slice's rank16 rows as boxes of
-      // 64, 32 and 16 rows; at most 3 per slice).
-      // gathered rows: this thread's 8 row addresses, loaded once per tile
-      const __nv_bfloat16 *xrow[RPT];
-#pragma unroll
-      for (int q = 0; q < RPT; ++q) {
-        const int r = (lt >> 3) + q * (LDT / 8);
-        xrow[q] = p.x + (!dense && r < len ? (int64_t)p.perm[start + r] * p.ldx : 0);
-      }
+      // rows past the tile's length read past the tensor's last row: zeros
+      int rr[4] = {0, 0, 0, 0};
       const CUtensorMap *bmap = nullptr;
       int bdst = 0, brow = 0;
-      if (p.tma_a && lt >= 1 && lt < 32) {
+      // consecutive token rows: one 128-row box (rows past len belong to other
+      // tokens and only reach accumulator rows that are never written)
+      const int t0 = p.perm[start];
+      const bool dense = p.perm[start + len - 1] - t0 == len - 1;
+      if (!aw) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = 4 * lane + e;
+          rr[e] = r < len ? p.perm[start + r] : p.T;
+        }
+      } else {
+        // lane b issues the stage's b-th adapter box (each slice's rank16 rows as
+        // boxes of 64, 32 and 16 rows; at most 24)
         int b = 0;
         for (int i = 0; i < p.n && !bmap; ++i)
           for (int j0 = 0; j0 < r16;) {
             const int hb = r16 - j0 >= 64 ? 64 : r16 - j0 >= 32 ? 32 : 16;
-            if (++b == lt) {
+            if (b++ == lane) {
               bmap = hb == 64 ? &tmA64 : hb == 32 ? &tmA32 : &tmA16;
               bdst = (i * r16 + j0) * 128;
               brow = i * p.R + j0;
@@ -458,180 +489,233 @@ __global__ void __launch_bounds__(ShCfg<QB>::THREADS, ShCfg<QB>::CTAS)
             j0 += hb;
           }
       }
+      const int aslot = p.a_one_slot ? 0 : slot;
+      const uint32_t tx = has_k ? (uint32_t)(TC_XB + ncols * KW * 2) : 0u;
       for (int k = kb; k < ke; ++k, ++g) {
+        if (g % nw != par) continue;              // another loader warp's stage
         const int s = g % NS;
         if (g >= NS && !wait_all(&empty[s], ((g / NS) & 1) ^ 1)) {
           ok = false;
           break;
         }
         uint8_t *st = ring + s * STAGE;
-        uint8_t *sa = st + SH_XB;
         const int k0 = k * KW;
-        const int64_t krem = p.in - k0 < (int64_t)KW ? p.in - k0 : (int64_t)KW;
-        const uint32_t nb = clamp16((int)krem * 2 - ch * 16);
-        if (lt == 0) {
-          if (tx) mbar_arrive_expect_tx(&full[s], tx);
-          else mbar_arrive(&full[s]);
-        }
-        __syncwarp();
-        if (lt == 0 && dense) tma_load_2d(st, &tmX, &full[s], k0, t0);
-        if (bmap) tma_load_3d(sa + bdst, bmap, &full[s], k0, brow, slot);
-        if (!dense) {
-#pragma unroll
-          for (int q = 0; q < RPT; ++q) {
-            const int r = (lt >> 3) + q * (LDT / 8);
-            cp_async16(st + swz(r, ch * 16, 128), xrow[q] + k0 + ch * 8, r < len ? nb : 0u);
+        if (!aw) {
+          if (lane == 0) {
+            if (tx) mbar_arrive_expect_tx(&full[s], tx);
+            else mbar_arrive(&full[s]);
           }
-        }
-        if (!p.tma_a) {
-          // rows j >= rank of a slice (padding, any value) are loaded too: their columns are dropped
-          for (int c = lt >> 3; c < ncols; c += LDT / 8) {
-            const int i = c / r16, j = c - i * r16;
-            const bool in_r = i * p.R + j < p.n * p.R;
-            cp_async16(sa + swz(c, ch * 16, 128), as + (int64_t)(in_r ? i * p.R + j : 0) * p.sa_row + k0 + ch * 8,
-                       in_r ? nb : 0u);
+          __syncwarp();
+          if (has_k) {
+            if (!dense) tma_gather4(st + lane * 512, &tmX, &full[s], k0, rr[0], rr[1], rr[2], rr[3]);
+            else if (lane == 0) tma_load_2d(st, &tmXd, &full[s], k0, t0);
           }
+        } else if (bmap && has_k) {
+          tma_load_3d(st + TC_XB + bdst, bmap, &full[s], k0, brow, aslot);
         }
-        cp_async_arrive(&full[s]);
       }
     }
-    pdl_launch_dependents();
-    return;
-  }
-
-  // ------------------------------------------------------------------ consumers
-  const int w = warp, rh = w & 1, cqt = w >> 1;   // 32-row half, column quarter
-  const int gq = lane >> 2, cq = lane & 3, l = lane;
-  int g = 0, nshared = 0;
-  bool ok = true;
-  for (int tau = s0.x; tau <= tlast && ok; ++tau) {
-    const int kb = tau == s0.x ? s0.y : 0, ke = tau == s1.x ? s1.y : nk;
-    const int4 td = p.tiles[tau];
-    const int slot = td.x, start = td.y, len = td.z;
-    const int rank = p.ranks[slot];
-    const int r16 = (rank + 15) & ~15;
-    const int nbt = p.n * r16 / 16;                 // 16-column blocks of this slot
-    const int nbq = (nbt + 3) / 4;                  // <= QB
-    const int cb0 = cqt * nbq, cb1 = min(nbt, cb0 + nbq);
-    const bool live = 32 * rh < len && cb0 < cb1;
-    float hacc[2][2 * QB][4];
+  } else if (any && warp == TC_MMA_WARP) {
+    // ---------------------------------------------------------------- MMA issuer (one thread)
+    if (lane == 0) {
+      int g = 0, seg = 0;
+      bool ok = true;
+      for (int tau = s0.x; tau <= tlast && ok; ++tau) {
+        const int kb = tau == s0.x ? s0.y : 0, ke = tau == s1.x ? s1.y : nk;
+        const int rank = p.ranks[p.tiles[tau].x];
+        const uint32_t idesc = tc_idesc_bf16(TC_M, p.n * ((rank + 15) & ~15));
+        // the previous segment's accumulator has been drained
+        if (seg > 0 && !mbar_wait(acce, (seg - 1) & 1)) break;
+        tc_fence_after();
+        for (int k = kb; k < ke; ++k, ++g) {
+          const int s = g % NS;
+          if (!mbar_wait(&full[s], (g / NS) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t xa = smem_u32(ring + s * STAGE), aa = xa + TC_XB;
 #pragma unroll
-    for (int m = 0; m < 2; ++m)
+          for (int kk = 0; kk < KW / 16; ++kk)
+            if ((int64_t)k * KW + kk * 16 < p.in)
+              tc_mma_bf16(tmem, tc_desc_sw128(xa + kk * 32), tc_desc_sw128(aa + kk * 32), idesc,
+                          (k > kb || kk > 0) ? 1u : 0u);
+          tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
+        }
+        if (!ok) break;
+        tc_commit(accf);
+        ++seg;
+      }
+      tc_commit(mdone);
+      mbar_wait(mdone, 0);
+    }
+    __syncwarp();
+  } else if (any) {
+    // ---------------------------------------------------------------- drain: one token row per thread
+    const int q = warp & 3, r = 32 * q + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+    int seg = 0, nshared = 0;
+    bool ok = true;
+    for (int tau = s0.x; tau <= tlast && ok; ++tau) {
+      const int kb = tau == s0.x ? s0.y : 0, ke = tau == s1.x ? s1.y : nk;
+      const int4 td = p.tiles[tau];
+      const int slot = td.x, start = td.y, len = td.z;
+      const int rank = p.ranks[slot];
+      const int r16 = (rank + 15) & ~15, ncols = p.n * r16;
+      if (!(ok = wait_all(accf, seg & 1))) break;
+      tc_fence_after();
+      const bool whole = kb == 0 && ke == nk;
+      float *hrow = r < len ? p.h + (int64_t)p.perm[start + r] * p.ldh : nullptr;
+      // partial sums column-major, [slot][column][128 rows]: a warp writes 128 bytes a column
+      float *pcol = whole ? nullptr
+                          : p.part + (size_t)(2 * blockIdx.x + (tau == s0.x ? 0 : 1)) * p.sh_nc * TC_M + r;
+      for (int c0 = 0; c0 < ncols; c0 += 16) {
+        float v[16];
+        if (has_k) {
+          tmem_ld16(trow + (uint32_t)c0, v);
+        } else {
 #pragma unroll
-      for (int t = 0; t < 2 * QB; ++t) hacc[m][t][0] = hacc[m][t][1] = hacc[m][t][2] = hacc[m][t][3] = 0.f;
-    for (int k = kb; k < ke; ++k, ++g) {
-      const int s = g % NS;
-      if (!(ok = wait_all(&full[s], (g / NS) & 1))) break;
-      const uint32_t xb = smem_u32(ring + s * STAGE), ab = xb + SH_XB;
-      const int k0 = k * KW;
-      if (live) {
+          for (int e = 0; e < 16; ++e) v[e] = 0.f;
+        }
+        const int i = c0 / r16, j0 = c0 - i * r16;
 #pragma unroll
-        for (int kk = 0; kk < KW / 16; ++kk) {
-          if (k0 + kk * 16 >= p.in) break;
-          uint32_t a[2][4];
+        for (int e = 0; e < 16; ++e)
+          if (j0 + e >= rank) v[e] = 0.f;   // columns past the rank come from padding rows of a
+        if (whole) {
+          if (hrow) {
+            float *hp = hrow + (int64_t)i * p.R + j0;
+            if (j0 + 16 <= rank) {
 #pragma unroll
-          for (int m = 0; m < 2; ++m)
-            ldsm_x4(xb + swz(32 * rh + 16 * m + (l & 15), (kk * 16 + ((l >> 4) << 3)) * 2, 128), a[m][0], a[m][1],
-                    a[m][2], a[m][3]);
+              for (int e = 0; e < 16; e += 4) *reinterpret_cast<float4 *>(hp + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+            } else {
 #pragma unroll
-          for (int q = 0; q < QB; ++q) {
-            if (cb0 + q >= cb1) break;
-            uint32_t b[4];
-            ldsm_x4(ab + swz((cb0 + q) * 16 + (l & 7) + ((l >> 4) << 3), (kk * 16 + (((l >> 3) & 1) << 3)) * 2, 128),
-                    b[0], b[1], b[2], b[3]);
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-              mma_bf16(hacc[m][2 * q], a[m], b[0], b[1]);
-              mma_bf16(hacc[m][2 * q + 1], a[m], b[2], b[3]);
+              for (int e = 0; e < 16; ++e)
+                if (j0 + e < rank) hp[e] = v[e];
             }
           }
+        } else if (r < len) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pcol[(size_t)(c0 + e) * TC_M] = v[e];
         }
       }
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-    }
-    if (!ok) break;
-    const bool whole = kb == 0 && ke == nk;
-    bool write = whole;
-    if (!whole) {
-      // a share of the tile: fp32 partial sums to this CTA's slot (0: its first tile, 1: its last)
-      float *part = p.part + (size_t)(2 * blockIdx.x + (tau == s0.x ? 0 : 1)) * MBM * p.sh_nc;
-      if (live) {
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-          for (int t = 0; t < 2 * QB; ++t) {
-            if (t >= 2 * (cb1 - cb0)) break;
-            const int r = 32 * rh + 16 * m + gq, c = cb0 * 16 + t * 8 + 2 * cq;
-            *reinterpret_cast<float2 *>(&part[r * p.sh_nc + c]) = make_float2(hacc[m][t][0], hacc[m][t][1]);
-            *reinterpret_cast<float2 *>(&part[(r + 8) * p.sh_nc + c]) = make_float2(hacc[m][t][2], hacc[m][t][3]);
-          }
-      }
+      if (lane == 0) mbar_arrive(acce);   // the accumulator may be overwritten
+      ++seg;
+      if (whole) continue;
+      // a share of the tile: publish the partial sums (stages done, on the tile's ticket)
       __threadfence();
       __syncwarp();
       if (lane == 0) mbar_arrive(pdone);
-      const uint32_t ph = nshared++ & 1;
-      if (threadIdx.x == 0) {
-        int last = 0;
-        if (mbar_wait(pdone, ph)) {
-          last = atomicAdd(&p.tickets[tau], ke - kb) + (ke - kb) == nk;
-          __threadfence();
-        }
-        *last_flag = last;
-        mbar_arrive(pflag);
+      if (warp == 4 && lane == 0) {
+        if (mbar_wait(pdone, nshared & 1)) atomicAdd(&p.tickets[tau], ke - kb);
       }
-      if (!(ok = wait_all(pflag, ph))) break;
-      write = *last_flag != 0;
-      if (write && live) {
-        // the owners of the tile are consecutive CTAs: add their partials in order
-        int bf = blockIdx.x;
-        while (bf > 0 && before(make_int2(tau, 0), p.starts[bf])) --bf;
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-          for (int t = 0; t < 2 * QB; ++t) hacc[m][t][0] = hacc[m][t][1] = hacc[m][t][2] = hacc[m][t][3] = 0.f;
-        for (int b = bf;; ++b) {
-          const int2 sb = p.starts[b];
-          if (b > bf && sb.x != tau) break;                 // past the tile's last owner
-          if (!before(sb, p.starts[b + 1])) continue;       // an empty share
-          const float *pb = p.part + (size_t)(2 * b + (sb.x == tau ? 0 : 1)) * MBM * p.sh_nc;
-#pragma unroll
-          for (int m = 0; m < 2; ++m)
-#pragma unroll
-            for (int t = 0; t < 2 * QB; ++t) {
-              if (t >= 2 * (cb1 - cb0)) break;
-              const int r = 32 * rh + 16 * m + gq, c = cb0 * 16 + t * 8 + 2 * cq;
-              const float2 v0 = __ldcg(reinterpret_cast<const float2 *>(&pb[r * p.sh_nc + c]));
-              const float2 v1 = __ldcg(reinterpret_cast<const float2 *>(&pb[(r + 8) * p.sh_nc + c]));
-              hacc[m][t][0] += v0.x; hacc[m][t][1] += v0.y; hacc[m][t][2] += v1.x; hacc[m][t][3] += v1.y;
-            }
-        }
-      }
-    }
-    // h rows < len, columns j < rank of each slice (columns past the rank come from padding rows of a)
-    if (write && live) {
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int r = 32 * rh + 16 * m + gq + 8 * hf;
-          if (r >= len) continue;
-          float *hrow = p.h + (int64_t)p.perm[start + r] * p.ldh;
-#pragma unroll
-          for (int t = 0; t < 2 * QB; ++t) {
-            if (t >= 2 * (cb1 - cb0)) break;
-            const int c = cb0 * 16 + t * 8 + 2 * cq, i = c / r16, j = c - i * r16;
-            float *hp2 = hrow + (int64_t)i * p.R + j;
-            if (j + 1 < rank) {
-              *reinterpret_cast<float2 *>(hp2) = make_float2(hacc[m][t][2 * hf], hacc[m][t][2 * hf + 1]);
-            } else if (j < rank) {
-              hp2[0] = hacc[m][t][2 * hf];
-            }
-          }
-        }
+      ++nshared;
     }
   }
+  // ------------------------------------------------------------------ final sums of shared tiles
+  // Every owner of a shared tile adds all owners' partial sums, in the owners'
+  // order, for its own slice of the tile's rows, once the tile's ticket shows all
+  // stages published.  Owners publish before they wait, so no wait depends on
+  // another.  All eight warps take part.
+  __syncthreads();
+  for (int pass = 0; any && pass < 2; ++pass) {
+    const int tau = pass == 0 ? s0.x : tlast;
+    if (pass == 1 && tlast == s0.x) break;
+    const int kb = tau == s0.x ? s0.y : 0, ke = tau == s1.x ? s1.y : nk;
+    if (kb == 0 && ke == nk) continue;           // a whole tile, already written
+    if (threadIdx.x == 0) {
+      int no = 0, me = 0;
+      const unsigned long long t0 = globaltimer();
+      for (uint32_t it = 0;; ++it) {
+        if (ld_acquire_gpu(&p.tickets[tau]) >= nk) break;
+        if ((it & 63u) == 63u && globaltimer() - t0 > kWaitLimitNs) {
+          flag_error(kErrWaitTimeout);
+          no = -1;
+          break;
+        }
+      }
+      if (no == 0) {
+        int bf = blockIdx.x;   // the owners are consecutive CTAs from the owner of the first stage
+        while (bf > 0 && before(make_int2(tau, 0), p.starts[bf])) --bf;
+        for (int b = bf;; ++b) {
+          const int2 sb = p.starts[b];
+          if (b > bf && sb.x != tau) break;            // past the tile's last owner
+          if (!before(sb, p.starts[b + 1])) continue;  // an empty share
+          if (no == TC_MAX_OWNERS) {
+            flag_error(kErrInternal);
+            no = -1;
+            break;
+          }
+          if (b == (int)blockIdx.x) me = no;
+          owners[no++] = 2 * b + (sb.x == tau ? 0 : 1);
+        }
+      }
+      last_flag[0] = no;
+      last_flag[1] = me;
+    }
+    __syncthreads();
+    const int no = last_flag[0], me = last_flag[1];
+    if (no > 0) {
+      const int4 td = p.tiles[tau];
+      const int start = td.y, len = td.z;
+      const int rank = p.ranks[td.x];
+      const int r16 = (rank + 15) & ~15, nq = p.n * r16 / 4;
+      const int r_lo = (int)((int64_t)len * me / no), r_hi = (int)((int64_t)len * (me + 1) / no);
+      const int nrows = r_hi - r_lo, nitems = nrows * nq;
+      // an item is 4 columns of one row, rows fastest (coalesced reads of the
+      // column-major partial sums); 4 items x 4 owners of loads in flight
+      for (int base = 0; base < nitems; base += TC_THREADS * 4) {
+        float acc[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+        for (int o0 = 0; o0 < no; o0 += 4) {
+          float u[4][4][4];
+#pragma unroll
+          for (int oo = 0; oo < 4; ++oo)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int item = base + j * TC_THREADS + threadIdx.x;
+              const bool live = o0 + oo < no && item < nitems;
+              const int row = r_lo + (live ? item % nrows : 0), c = live ? 4 * (item / nrows) : 0;
+              const float *pc = p.part + ((size_t)owners[live ? o0 + oo : 0] * p.sh_nc + c) * TC_M + row;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) u[oo][j][e] = live ? __ldcg(pc + (size_t)e * TC_M) : 0.f;
+            }
+#pragma unroll
+          for (int oo = 0; oo < 4; ++oo)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[j][e] += u[oo][j][e];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int item = base + j * TC_THREADS + threadIdx.x;
+          if (item >= nitems) continue;
+          const int row = r_lo + item % nrows, c = 4 * (item / nrows);
+          const int i = c / r16, jj = c - i * r16;
+          float *hp = p.h + (int64_t)p.perm[start + row] * p.ldh + (int64_t)i * p.R + jj;
+          if (jj + 4 <= rank) {
+            *reinterpret_cast<float4 *>(hp) = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (jj + e < rank) hp[e] = acc[j][e];
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
   pdl_launch_dependents();
+  // every MMA has completed (the issuer waited for its last commit): free the tensor memory
+  tc_fence_before();
+  __syncthreads();
+  if (warp == TC_MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, (uint32_t)p.tc_cols);
+  }
 }
 
 // =============================================================================
@@ -666,7 +750,9 @@ __global__ void __launch_bounds__(ExCfg<RP>::THREADS, RP >= 128 ? 2 : 3)
   uint64_t *freeb = done + NS;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x / p.ngroups, grp = blockIdx.x % p.ngroups;
+  // CTA (tile, group, 64-row sub-tile)
+  const int sub = blockIdx.x % p.nsub, rest = blockIdx.x / p.nsub;
+  const int tile = rest / p.ngroups, grp = rest % p.ngroups;
   pdl_wait();
   if (tile >= p.header[1]) return;
   // group -> (slice i, first block b0, number of blocks nb)
@@ -683,7 +769,8 @@ __global__ void __launch_bounds__(ExCfg<RP>::THREADS, RP >= 128 ? 2 : 3)
   }
   if (i >= p.n || nb <= 0) return;
   const int4 td = p.tiles[tile];
-  const int slot = td.x, start = td.y, len = td.z;
+  const int slot = td.x, start = td.y + MBM * sub, len = min(MBM, td.z - MBM * sub);
+  if (len <= 0) return;
   const int rank = p.ranks[slot];
   const int rank8 = (rank + 7) & ~7;
   const int col_end = p.off[i + 1];
@@ -917,7 +1004,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t *__restrict__
 // ----------------------------------------------------------------------------- host side
 namespace {
 
-int max_tiles(int64_t T, int S) { return (int)(ceil_div(T, MBM) + std::min<int64_t>(S, T)); }
+// Tiles of at most TC_M tokens of one slot: at most one partial tile per slot.
+int max_tiles(int64_t T, int S) { return (int)(ceil_div(T, TC_M) + std::min<int64_t>(S, T)); }
 
 struct SchedPtrs {
   int *header, *counts;
@@ -941,12 +1029,12 @@ struct ShrinkWs {
 int shrink_nc_bound(int R) { return (int)std::min<int64_t>(kMaxHC, (int64_t)LORA_MAX_SLICES * round_up(R, 16)); }
 size_t shrink_ws_bytes(int64_t T, int S, int R) {
   return ws_round((size_t)(SH_MAX_CTAS + 1) * 8) + ws_round((size_t)max_tiles(T, S) * 4) +
-         ws_round((size_t)2 * SH_MAX_CTAS * MBM * shrink_nc_bound(R) * 4);
+         ws_round((size_t)2 * SH_MAX_CTAS * TC_M * shrink_nc_bound(R) * 4);
 }
 bool carve_shrink(WsCarver &c, int64_t T, int S, int R, ShrinkWs &sw) {
   sw.starts = (int2 *)c.take((size_t)(SH_MAX_CTAS + 1) * 8);
   sw.tickets = (int *)c.take((size_t)max_tiles(T, S) * 4);
-  sw.part = (float *)c.take((size_t)2 * SH_MAX_CTAS * MBM * shrink_nc_bound(R) * 4);
+  sw.part = (float *)c.take((size_t)2 * SH_MAX_CTAS * TC_M * shrink_nc_bound(R) * 4);
   return sw.starts && sw.tickets && sw.part;
 }
 
@@ -960,14 +1048,14 @@ bool carve_sched(WsCarver &c, int64_t T, int S, SchedPtrs &sp) {
 
 lora_status_t launch_group(const lora_addressing_t &ad, const int32_t *ranks, int32_t *counts, int32_t *perm,
                            int32_t *num_active, int *header, int4 *tiles, cudaStream_t st,
-                           SplitOut so = SplitOut{nullptr, nullptr, 0, 0, 0, 0}) {
+                           SplitOut so = SplitOut{nullptr, nullptr, 0, 0, 0, 0, 0}) {
   const int S = ad.num_slots;
   int nw = (int)std::max<int64_t>(1, (160 * 1024 / 4 - 256 - 3 * S) / S);   // shared-memory bound
   nw = std::min<int64_t>({nw, 32, std::max<int64_t>(1, ceil_div(ad.num_tokens, LORA_GROUP_TOKENS_PER_WARP))});
   const size_t smem = (size_t)(nw * S + 3 * S + 161) * 4;
   LORA_CUDA(ensure_smem((const void *)group_kernel, smem));
   LORA_CUDA(launch(group_kernel, dim3(1), dim3(nw * 32), smem, st, 1, true, ad.slots, ad.num_tokens, S,
-                   ad.max_rank, ranks, counts, perm, num_active, header, tiles, (int)MBM, so));
+                   ad.max_rank, ranks, counts, perm, num_active, header, tiles, (int)TC_M, so));
   return LORA_OK;
 }
 
@@ -988,53 +1076,63 @@ bool map_adapter(CUtensorMap *m, const void *base, int64_t S, int64_t rows, int6
   return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// 16-column blocks per consumer quarter of the shrink for the widest slot.
-int shrink_qb(int n, int R) { return (int)std::min<int64_t>(4, ceil_div((int64_t)n * round_up(R, 16) / 16, 4)); }
+// Boxes of `box_rows` rows x 64 columns of a row-major [rows][cols] operand (128-byte swizzle).
+bool map_box(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows) {
+  uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+  uint64_t str[1] = {(uint64_t)ld * 2};
+  uint32_t box[2] = {64, box_rows};
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
 
-template <int QB>
+// Rows of x, one 64-column box a row (the four-row gather copies of the shrink).
+bool map_gather_rows(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld) {
+  uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+  uint64_t str[1] = {(uint64_t)ld * 2};
+  uint32_t box[2] = {64, 1};
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Cost of a stage in the work split: n * rank16 adapter rows plus this weight for
+// the tile's x rows (128-byte rows).
+#ifndef LORA_SHRINK_XW
+#define LORA_SHRINK_XW TC_M
+#endif
+
 int shrink_grid() {
-  const int occ = occupancy((const void *)shrink_kernel<QB>, ShCfg<QB>::THREADS, ShCfg<QB>::BYTES);
+  const int occ = occupancy((const void *)shrink_kernel, TC_THREADS, TC_BYTES);
   return (int)std::min<int64_t>(SH_MAX_CTAS, std::max<int64_t>(1, (int64_t)occ * num_sms()));
 }
-int shrink_grid(int n, int R) {
-  switch (shrink_qb(n, R)) {
-    case 1: return shrink_grid<1>();
-    case 2: return shrink_grid<2>();
-    case 3: return shrink_grid<3>();
-    default: return shrink_grid<4>();
-  }
-}
 
-template <int QB>
 lora_status_t launch_shrink(MArgs a, int64_t T, int G, cudaStream_t st) {
-  auto kern = shrink_kernel<QB>;
-  const size_t smem = ShCfg<QB>::BYTES;
-  LORA_CUDA(ensure_smem((const void *)kern, smem));
-  CUtensorMap tmX, tmA16, tmA32, tmA64;
-  a.tma_ok = map_rows(&tmX, a.x, T, a.in, a.ldx) ? 1 : 0;
-  const int64_t arows = (int64_t)a.n * a.R;
-  a.tma_a = map_adapter(&tmA16, a.a, a.S, arows, a.in, a.sa_slot, a.sa_row, 16) &&
-                    map_adapter(&tmA32, a.a, a.S, arows, a.in, a.sa_slot, a.sa_row, 32) &&
-                    map_adapter(&tmA64, a.a, a.S, arows, a.in, a.sa_slot, a.sa_row, 64)
-                ? 1
-                : 0;
+  LORA_CUDA(ensure_smem((const void *)shrink_kernel, TC_BYTES));
+  CUtensorMap tmX, tmXd, tmA16, tmA32, tmA64;
+  memset(&tmX, 0, sizeof(tmX));
+  memset(&tmXd, 0, sizeof(tmXd));
+  memset(&tmA16, 0, sizeof(tmA16));
+  memset(&tmA32, 0, sizeof(tmA32));
+  memset(&tmA64, 0, sizeof(tmA64));
+  a.T = (int)T;
   const int nc = a.n * (int)round_up(a.R, 16);   // most columns a slot can have
   a.sh_nc = nc;
-  a.sh_stage = SH_XB + nc * KW * 2;
-  a.sh_ns = std::min(16, ShCfg<QB>::RING / a.sh_stage);
-  if (a.sh_ns < 2 || nc > shrink_nc_bound(a.R)) return LORA_ERR_UNSUPPORTED;
-  LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(ShCfg<QB>::THREADS), smem, st, 1, true, tmX, tmA16, tmA32, tmA64,
-                   a));
-  return LORA_OK;
-}
-
-lora_status_t dispatch_shrink(const MArgs &a, int64_t T, int G, cudaStream_t st) {
-  switch (shrink_qb(a.n, a.R)) {
-    case 1: return launch_shrink<1>(a, T, G, st);
-    case 2: return launch_shrink<2>(a, T, G, st);
-    case 3: return launch_shrink<3>(a, T, G, st);
-    default: return launch_shrink<4>(a, T, G, st);
+  a.tc_cols = 32;
+  while (a.tc_cols < nc) a.tc_cols *= 2;
+  a.sh_stage = TC_XB + nc * KW * 2;
+  a.sh_ns = std::min(16, TC_RING / a.sh_stage);
+  if (a.sh_ns < 2 || nc > shrink_nc_bound(a.R) || a.tc_cols > 512) return LORA_ERR_UNSUPPORTED;
+  if (a.in > 0) {
+    // one adapter when the slot stride is zero: a map over one slot, slot coordinate 0
+    a.a_one_slot = a.sa_slot == 0 ? 1 : 0;
+    const int64_t arows = (int64_t)a.n * a.R, aS = a.a_one_slot ? 1 : a.S;
+    const int64_t sslot = a.a_one_slot ? arows * a.sa_row : a.sa_slot;
+    if (!map_gather_rows(&tmX, a.x, T, a.in, a.ldx) || !map_box(&tmXd, a.x, T, a.in, a.ldx, TC_M) ||
+        !map_adapter(&tmA16, a.a, aS, arows, a.in, sslot, a.sa_row, 16) ||
+        !map_adapter(&tmA32, a.a, aS, arows, a.in, sslot, a.sa_row, 32) ||
+        !map_adapter(&tmA64, a.a, aS, arows, a.in, sslot, a.sa_row, 64))
+      return LORA_ERR_ALIGNMENT;
   }
+  LORA_CUDA(launch(shrink_kernel, dim3((unsigned)G), dim3(TC_THREADS), TC_BYTES, st, 1, true, tmX, tmXd, tmA16,
+                   tmA32, tmA64, a));
+  return LORA_OK;
 }
 
 template <int RP>
@@ -1047,15 +1145,17 @@ lora_status_t launch_expand(MArgs a, int64_t T, cudaStream_t st) {
   int64_t blocks = 0;
   for (int i = 0; i < a.n; ++i) blocks += ceil_div(a.off[i + 1] - a.off[i], CBW);
   // column blocks per CTA: about three waves of CTAs over the tile bound
-  const int64_t gb = std::max<int64_t>(1, ceil_div(tiles * blocks, 3 * cap));
+  const int64_t gb = std::max<int64_t>(1, ceil_div(tiles * (TC_M / MBM) * blocks, 3 * cap));
   int64_t ng = 0;
   for (int i = 0; i < a.n; ++i) ng += ceil_div(ceil_div(a.off[i + 1] - a.off[i], CBW), gb);
   if (ng == 0) return LORA_OK;
   a.gb = (int)gb;
   a.ngroups = (int)ng;
+  a.nsub = TC_M / MBM;
   CUtensorMap tmY;
   a.tma_ok = map_rows(&tmY, a.y, T, a.off[a.n], a.ldy) ? 1 : 0;
-  LORA_CUDA(launch(kern, dim3((unsigned)(tiles * ng)), dim3(ExCfg<RP>::THREADS), smem, st, 1, true, tmY, a));
+  LORA_CUDA(launch(kern, dim3((unsigned)(tiles * ng * a.nsub)), dim3(ExCfg<RP>::THREADS), smem, st, 1, true, tmY,
+                   a));
   return LORA_OK;
 }
 
@@ -1116,7 +1216,7 @@ MArgs margs(const MultiArgs &m, const SchedPtrs &sp) {
 }
 
 lora_status_t schedule(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, cudaStream_t st,
-                       SplitOut so = SplitOut{nullptr, nullptr, 0, 0, 0, 0}) {
+                       SplitOut so = SplitOut{nullptr, nullptr, 0, 0, 0, 0, 0}) {
   if (!carve_sched(c, m.addr.num_tokens, m.addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
   return launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st, so);
 }
@@ -1129,9 +1229,9 @@ lora_status_t schedule_and_shrink(const MultiArgs &m, WsCarver &c, SchedPtrs &sp
   if (!carve_sched(c, T, S, sp)) return LORA_ERR_WORKSPACE;
   ShrinkWs sw;
   if (!carve_shrink(c, T, S, R, sw)) return LORA_ERR_WORKSPACE;
-  const int G = shrink_grid(m.n, R);
+  const int G = shrink_grid();
   const int nk = (int)std::max<int64_t>(1, ceil_div(m.in, KW));
-  SplitOut so{sw.starts, sw.tickets, G, m.n, nk, max_tiles(T, S)};
+  SplitOut so{sw.starts, sw.tickets, G, m.n, nk, max_tiles(T, S), LORA_SHRINK_XW};
   LORA_TRY(launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st, so));
   MArgs a = margs(m, sp);
   a.h = h;
@@ -1141,7 +1241,7 @@ lora_status_t schedule_and_shrink(const MultiArgs &m, WsCarver &c, SchedPtrs &sp
   a.part = sw.part;
   a.nk = nk;
   *out = a;
-  return dispatch_shrink(a, T, G, st);
+  return launch_shrink(a, T, G, st);
 }
 
 }  // namespace
