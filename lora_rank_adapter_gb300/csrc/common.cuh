@@ -175,6 +175,13 @@ __device__ __forceinline__ float2 ld_dsmem_f2(const void *local_ptr, uint32_t ct
   asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(remote) : "memory");
   return v;
 }
+__device__ __forceinline__ float ld_dsmem_f1(const void *local_ptr, uint32_t cta) {
+  uint32_t local = smem_u32(local_ptr), remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(cta));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
+  return v;
+}
 // Named barrier among `threads` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

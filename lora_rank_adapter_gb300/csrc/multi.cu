@@ -58,14 +58,11 @@ struct MArgs {
   int tma_ok;                     // the tensor maps of x / y are valid
   int tma_a;                      // the tensor map of a is valid (shrink)
   int sh_ns, sh_stage;            // shrink: stages in the ring, bytes per stage
-  int sh_nc, nk;                  // shrink: partial-sum row pitch (columns), stages per tile
+  int nk;                         // shrink: stages (64 columns of `in`) per tile
   int T;                          // number of tokens (rows of x)
   int tc_cols;                    // shrink: tensor-memory columns of the accumulator
   int a_one_slot;                 // shrink: the adapter map has one slot (slot stride 0)
   int nsub;                       // expand: 64-row sub-tiles per tile
-  const int2 *starts;             // shrink: first (tile, stage) of each CTA, [G + 1]
-  int *tickets;                   // shrink: stages finished per tile
-  float *part;                    // shrink: partial sums, [2 G][64][sh_nc]
 };
 
 // Byte offset of (row, col) in a 64 x 64 bf16 tile written by TMA with the
@@ -92,10 +89,6 @@ template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
 
 // Warp-uniform bounded wait: lane 0 polls the barrier, the warp barrier then
 // orders what lane 0 observed before every lane's later reads.
@@ -114,11 +107,7 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
 #endif
 }
 
-// A operand (16x16 at rows r0.., cols c0..) / B operands (two n8 tiles) from padded rows.
-__device__ __forceinline__ void lda_p(uint32_t base, int pitch, int r0, int c0, uint32_t (&a)[4]) {
-  const int l = lane_id();
-  ldsm_x4(base + (r0 + (l & 15)) * pitch + (c0 + ((l >> 4) << 3)) * 2, a[0], a[1], a[2], a[3]);
-}
+// B operands (two n8 tiles) from padded rows.
 __device__ __forceinline__ void ldb_p(uint32_t base, int pitch, int n0, int k0, uint32_t (&b)[4]) {
   const int l = lane_id();
   ldsm_x4(base + (n0 + (l & 7) + ((l >> 4) << 3)) * pitch + (k0 + (((l >> 3) & 1) << 3)) * 2, b[0], b[1], b[2],
@@ -185,32 +174,21 @@ __device__ __forceinline__ void block_scan2(int a, int b, int &ea, int &eb, int 
 }
 
 constexpr int GU = 8;   // tokens per lane per batch in group_kernel
-
-// Optional output of the grouping for the shrink: the split of its work over G
-// persistent CTAs.  Tile tau costs nk stages of n * rank16(slot) + xw rows of
-// 128 bytes (a rows of every slice plus x rows); CTA b starts at the first
-// (tile, stage) whose cost offset is at least floor(total * b / G).
-struct SplitOut {
-  int2 *starts;    // [G + 1] (tile, stage); starts[G] = (tiles, 0)
-  int *tickets;    // [ntick] zeroed: stages of a tile finished so far
-  int G, n, nk, ntick, xw;   // xw: x rows of a tile per stage
-};
 // Tokens per warp the grouping aims for (fewer warps: shorter scans and barriers).
 #ifndef LORA_GROUP_TOKENS_PER_WARP
 #define LORA_GROUP_TOKENS_PER_WARP 256
 #endif
 
+
 __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__ slots, int T, int S, int R,
                                                      const int32_t *__restrict__ ranks, int32_t *counts_out,
                                                      int32_t *perm_out, int32_t *num_active_out, int *header,
-                                                     int4 *tiles, int bmt, SplitOut so) {
+                                                     int4 *tiles, int bmt) {
   extern __shared__ int gsm[];
   const int nw = blockDim.x >> 5;
   int *hist = gsm;                 // [nw][S]
   int *srank = gsm + nw * S;       // [S]
   int *sh = srank + S;             // scan scratch (160 ints)
-  int *stb = sh + 160;             // [S] first tile of each slot
-  int *spc = stb + S;              // [S + 1] cost prefix of each slot (per stage)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
   const int t_lo = (int)((int64_t)T * warp / nw), t_hi = (int)((int64_t)T * (warp + 1) / nw);
@@ -243,7 +221,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
     }
   }
   __syncthreads();
-  int run = 0, trun = 0, crun = 0;
+  int run = 0, trun = 0;
   for (int c0 = 0; c0 < S; c0 += blockDim.x) {
     const int s = c0 + threadIdx.x;
     int cnt = 0;
@@ -262,51 +240,9 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
         cur += hcount;
       }
       for (int i = 0; i < nt; ++i) tiles[tb + i] = make_int4(s, base + i * bmt, min(bmt, cnt - i * bmt), 0);
-      stb[s] = tb;
     }
     run += tc;
     trun += tt;
-    if (so.G > 0) {
-      const int cost = s < S ? nt * (so.n * ((srank[s] + 15) & ~15) + so.xw) : 0;
-      int ecost, dummy, tcost, tdummy;
-      block_scan2(cost, 0, ecost, dummy, tcost, tdummy, sh);
-      if (s < S) spc[s] = crun + ecost;
-      crun += tcost;
-    }
-  }
-  if (so.G > 0) {
-    if (threadIdx.x == 0) spc[S] = crun;
-    for (int i = threadIdx.x; i < so.ntick; i += blockDim.x) so.tickets[i] = 0;
-    __syncthreads();
-    const int64_t total = (int64_t)crun * so.nk;
-    // every share holds at least nk / 32 stages of the widest slot, so a tile has
-    // at most 33 owners; CTAs past the shares used get none
-    const int64_t wmax = (int64_t)so.n * ((R + 15) & ~15) + so.xw;
-    const int64_t min_share = (int64_t)((so.nk + 31) / 32) * wmax;
-    const int Gu = (int)max((int64_t)1, min((int64_t)so.G, total / min_share));
-    for (int b = threadIdx.x; b <= so.G; b += blockDim.x) {
-      const int64_t c = b >= Gu ? total : total * b / Gu;
-      int tau = trun, k = 0;
-      if (c < total) {
-        int lo = 0, hi = S - 1;   // the last slot whose cost starts at or before c
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if ((int64_t)spc[mid] * so.nk <= c) lo = mid;
-          else hi = mid - 1;
-        }
-        const int64_t w = so.n * ((srank[lo] + 15) & ~15) + so.xw;
-        const int64_t o = c - (int64_t)spc[lo] * so.nk;
-        int64_t ti = o / (so.nk * w);
-        int64_t kk = (o - ti * so.nk * w + w - 1) / w;
-        if (kk >= so.nk) {
-          ++ti;
-          kk = 0;
-        }
-        tau = stb[lo] + (int)ti;
-        k = (int)kk;
-      }
-      so.starts[b] = make_int2(tau, k);
-    }
   }
   if (threadIdx.x == 0) {
     *num_active_out = run;
@@ -358,45 +294,30 @@ constexpr int RPT = MBM * 8 / LDT;     // tile rows handled per loader thread (8
 // =============================================================================
 // shrink_kernel: h[t, i*R + j] = x[t] . a[slot][i*R + j] for every slice i and
 // j < rank, over the slot-sorted tiles of at most 128 tokens, on the
-// fifth-generation tensor cores.  The work, tiles x stages of 64 columns of
-// `in`, is split over persistent CTAs (one per SM) by cost: the grouping kernel
-// writes each CTA's first (tile, stage), so every CTA streams about the same
-// number of bytes whatever the ranks.  A warp keeps one tensor-copy instruction
-// in flight at a time (its lanes' copies run together), so the stages are dealt
+// fifth-generation tensor cores.  One tile per cluster of `cl` CTAs; CTA q of
+// the cluster takes stages [nk q / cl, nk (q + 1) / cl) of the contraction (64
+// columns of `in` a stage).  A warp keeps one tensor-copy instruction in flight
+// at a time (its lanes' copies run together), so the stages are dealt
 // round-robin to several loader warps: x loaders take the tile's 128 x rows (one
 // 128-row box when the tile's tokens are consecutive rows, else lane q gathers
 // rows 4q..4q+3 with one four-row gather copy), adapter loaders the first rank16
 // rows of every slice of a[slot] (lane b: the b-th box of 64, 32 or 16 rows),
-// all with the 128-byte swizzle, into a ring that runs on across tiles.  Lane 0
-// of the MMA warp issues four 128 x (n * rank16) x 16 MMAs per stage into a
-// tensor-memory accumulator (x read once per tile for all slices); warps 4-7
-// drain the accumulator, one token row per thread.  A tile wholly inside one CTA's share
-// is written to h directly; a tile shared by several CTAs leaves fp32 partial
-// sums in the workspace, and the CTA that completes its stages (atomic ticket)
-// adds them in the owners' order, so the result does not depend on timing.
+// all with the 128-byte swizzle.  Lane 0 of the MMA warp issues four
+// 128 x (n * rank16) x 16 MMAs per stage into a tensor-memory accumulator (x read
+// once per tile for all slices); warps 4-7 drain it, one token row per thread.
+// CTAs q > 0 leave their partial sums in their own shared memory; CTA 0 adds
+// them to its own through distributed shared memory in cluster-rank order, so
+// the result does not depend on timing.
 // =============================================================================
 constexpr int TC_M = 128;                  // tokens per tile (accumulator rows)
 constexpr int TC_XB = TC_M * KW * 2;       // x bytes of one stage (16 KB)
 // Warp roles: x loaders [0, TC_XW), drain [4, 8), the MMA warp, adapter loaders
-// [TC_AW0, TC_AW0 + TC_AW).  Two CTAs an SM (smaller ring, fewer loader warps)
-// overlap one CTA's prologue, drains and final sums with the other's streaming.
-#ifndef LORA_SHRINK_2CTA
-#define LORA_SHRINK_2CTA 0
-#endif
-#if LORA_SHRINK_2CTA
-constexpr int TC_CTAS = 2, TC_THREADS = 256, TC_XW = 2, TC_MMA_WARP = 2, TC_AW0 = 3, TC_AW = 1;
-constexpr int TC_RING = 108 * 1024;
-#else
-constexpr int TC_CTAS = 1, TC_THREADS = 352, TC_XW = 4, TC_MMA_WARP = 8, TC_AW0 = 9, TC_AW = 2;
+// [TC_AW0, TC_AW0 + TC_AW).
+constexpr int TC_THREADS = 352, TC_XW = 4, TC_MMA_WARP = 8, TC_AW0 = 9, TC_AW = 2;
 constexpr int TC_RING = 200 * 1024;
-#endif
-constexpr int TC_MAX_OWNERS = 64;          // owners of a shared tile listed for the final sum
 constexpr int TC_BYTES = 1024 + 1024 + TC_RING;
-constexpr int SH_MAX_CTAS = 160;           // bound on the persistent grid (partial-sum workspace)
 
-__device__ __forceinline__ bool before(int2 u, int2 v) { return u.x < v.x || (u.x == v.x && u.y < v.y); }
-
-__global__ void __launch_bounds__(TC_THREADS, TC_CTAS)
+__global__ void __launch_bounds__(TC_THREADS, 1)
     shrink_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXd,
                   const __grid_constant__ CUtensorMap tmA16, const __grid_constant__ CUtensorMap tmA32,
                   const __grid_constant__ CUtensorMap tmA64, MArgs p) {
@@ -404,15 +325,16 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS)
   uint8_t *base = align1024(smem_raw);
   uint64_t *full = reinterpret_cast<uint64_t *>(base);
   uint64_t *empty = full + 16;
-  uint64_t *accf = empty + 16, *acce = accf + 1;       // accumulator written / drained
-  uint64_t *pdone = acce + 1, *pflag = pdone + 1;      // hand-off of a shared tile's partial sums
-  uint64_t *mdone = pflag + 1;                         // every MMA of this CTA has completed
-  volatile int *last_flag = reinterpret_cast<volatile int *>(mdone + 1);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mdone + 2);
-  int *owners = reinterpret_cast<int *>(mdone + 3);   // [TC_MAX_OWNERS] partial slots of the owners, in order
+  uint64_t *accf = empty + 16;                         // accumulator written
+  uint64_t *xready = accf + 1, *xdone = xready + 1;    // partial sums in shared memory / read by CTA 0
+  uint64_t *mdone = xdone + 1;                         // every MMA of this CTA has completed
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mdone + 1);
   uint8_t *ring = base + 1024;
-  const int NS = p.sh_ns, STAGE = p.sh_stage, nk = p.nk;
+  float *xbuf = reinterpret_cast<float *>(ring);       // [column][128 rows] once the ring is drained
+  const int NS = p.sh_ns, STAGE = p.sh_stage, nk = p.nk, cl = p.cl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x / cl;
+  const uint32_t q = cl > 1 ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -420,22 +342,28 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS)
       mbar_init(&empty[s], 1);
     }
     mbar_init(accf, 1);
-    mbar_init(acce, 4);
-    mbar_init(pdone, 4);
-    mbar_init(pflag, 1);
+    mbar_init(xready, cl > 1 ? 128 * (cl - 1) : 1);   // every drain thread of every other CTA
+    mbar_init(xdone, 128);                             // every drain thread of CTA 0
     mbar_init(mdone, 1);
     fence_barrier_init();
   }
   if (warp == TC_MMA_WARP) tmem_alloc(tmem_slot, (uint32_t)p.tc_cols);
   tc_fence_before();
-  __syncthreads();
+  if (cl > 1) cluster_sync_all(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
-  const int2 s0 = p.starts[blockIdx.x], s1 = p.starts[blockIdx.x + 1];
-  const bool any = before(s0, s1);
-  const int tlast = s1.y > 0 ? s1.x : s1.x - 1;      // last tile with a stage of this CTA
+  const bool any = tile < p.header[1];                // the whole cluster alike
+  const int kb = (int)((int64_t)nk * q / cl), ke = (int)((int64_t)nk * (q + 1) / cl);
   const bool has_k = p.in > 0;
+  int4 td = make_int4(0, 0, 0, 0);
+  int rank = 0;
+  if (any) {
+    td = p.tiles[tile];
+    rank = p.ranks[td.x];
+  }
+  const int slot = td.x, start = td.y, len = td.z;
+  const int r16 = (rank + 15) & ~15, ncols = p.n * r16;
 
   const bool aw = warp >= TC_AW0 && warp < TC_AW0 + TC_AW;   // adapter loader
   if (any && (warp < TC_XW || aw)) {
@@ -451,262 +379,142 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS)
         prefetch_tmap(&tmXd);
       }
     }
-    int g = 0;
-    bool ok = true;
-    for (int tau = s0.x; tau <= tlast && ok; ++tau) {
-      const int kb = tau == s0.x ? s0.y : 0, ke = tau == s1.x ? s1.y : nk;
-      const int4 td = p.tiles[tau];
-      const int slot = td.x, start = td.y, len = td.z;
-      const int rank = p.ranks[slot];
-      const int r16 = (rank + 15) & ~15, ncols = p.n * r16;
-      // rows past the tile's length read past the tensor's last row: zeros
-      int rr[4] = {0, 0, 0, 0};
-      const CUtensorMap *bmap = nullptr;
-      int bdst = 0, brow = 0;
-      // consecutive token rows: one 128-row box (rows past len belong to other
-      // tokens and only reach accumulator rows that are never written)
-      const int t0 = p.perm[start];
-      const bool dense = p.perm[start + len - 1] - t0 == len - 1;
-      if (!aw) {
+    // consecutive token rows: one 128-row box (rows past len belong to other
+    // tokens, or lie past the last row and read as zeros, and only reach
+    // accumulator rows that are never written)
+    const int t0 = p.perm[start];
+    const bool dense = p.perm[start + len - 1] - t0 == len - 1;
+    int rr[4] = {0, 0, 0, 0};
+    const CUtensorMap *bmap = nullptr;
+    int bdst = 0, brow = 0;
+    if (!aw) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = 4 * lane + e;
-          rr[e] = r < len ? p.perm[start + r] : p.T;
-        }
-      } else {
-        // lane b issues the stage's b-th adapter box (each slice's rank16 rows as
-        // boxes of 64, 32 and 16 rows; at most 24)
-        int b = 0;
-        for (int i = 0; i < p.n && !bmap; ++i)
-          for (int j0 = 0; j0 < r16;) {
-            const int hb = r16 - j0 >= 64 ? 64 : r16 - j0 >= 32 ? 32 : 16;
-            if (b++ == lane) {
-              bmap = hb == 64 ? &tmA64 : hb == 32 ? &tmA32 : &tmA16;
-              bdst = (i * r16 + j0) * 128;
-              brow = i * p.R + j0;
-              break;
-            }
-            j0 += hb;
-          }
+      for (int e = 0; e < 4; ++e) {
+        const int r = 4 * lane + e;
+        rr[e] = r < len ? p.perm[start + r] : p.T;   // past the last row: zeros
       }
-      const int aslot = p.a_one_slot ? 0 : slot;
-      const uint32_t tx = has_k ? (uint32_t)(TC_XB + ncols * KW * 2) : 0u;
-      for (int k = kb; k < ke; ++k, ++g) {
-        if (g % nw != par) continue;              // another loader warp's stage
-        const int s = g % NS;
-        if (g >= NS && !wait_all(&empty[s], ((g / NS) & 1) ^ 1)) {
-          ok = false;
-          break;
-        }
-        uint8_t *st = ring + s * STAGE;
-        const int k0 = k * KW;
-        if (!aw) {
-          if (lane == 0) {
-            if (tx) mbar_arrive_expect_tx(&full[s], tx);
-            else mbar_arrive(&full[s]);
+    } else {
+      // lane b issues the stage's b-th adapter box (each slice's rank16 rows as
+      // boxes of 64, 32 and 16 rows; at most 24)
+      int b = 0;
+      for (int i = 0; i < p.n && !bmap; ++i)
+        for (int j0 = 0; j0 < r16;) {
+          const int hb = r16 - j0 >= 64 ? 64 : r16 - j0 >= 32 ? 32 : 16;
+          if (b++ == lane) {
+            bmap = hb == 64 ? &tmA64 : hb == 32 ? &tmA32 : &tmA16;
+            bdst = (i * r16 + j0) * 128;
+            brow = i * p.R + j0;
+            break;
           }
-          __syncwarp();
-          if (has_k) {
-            if (!dense) tma_gather4(st + lane * 512, &tmX, &full[s], k0, rr[0], rr[1], rr[2], rr[3]);
-            else if (lane == 0) tma_load_2d(st, &tmXd, &full[s], k0, t0);
-          }
-        } else if (bmap && has_k) {
-          tma_load_3d(st + TC_XB + bdst, bmap, &full[s], k0, brow, aslot);
+          j0 += hb;
         }
+    }
+    const int aslot = p.a_one_slot ? 0 : slot;
+    const uint32_t tx = has_k ? (uint32_t)(TC_XB + ncols * KW * 2) : 0u;
+    for (int k = kb, g = 0; k < ke; ++k, ++g) {
+      if (g % nw != par) continue;              // another loader warp's stage
+      const int s = g % NS;
+      if (g >= NS && !wait_all(&empty[s], ((g / NS) & 1) ^ 1)) break;
+      uint8_t *st = ring + s * STAGE;
+      const int k0 = k * KW;
+      if (!aw) {
+        if (lane == 0) {
+          if (tx) mbar_arrive_expect_tx(&full[s], tx);
+          else mbar_arrive(&full[s]);
+        }
+        __syncwarp();
+        if (has_k) {
+          if (!dense) tma_gather4(st + lane * 512, &tmX, &full[s], k0, rr[0], rr[1], rr[2], rr[3]);
+          else if (lane == 0) tma_load_2d(st, &tmXd, &full[s], k0, t0);
+        }
+      } else if (bmap && has_k) {
+        tma_load_3d(st + TC_XB + bdst, bmap, &full[s], k0, brow, aslot);
       }
     }
   } else if (any && warp == TC_MMA_WARP) {
     // ---------------------------------------------------------------- MMA issuer (one thread)
     if (lane == 0) {
-      int g = 0, seg = 0;
+      const uint32_t idesc = tc_idesc_bf16(TC_M, ncols);
       bool ok = true;
-      for (int tau = s0.x; tau <= tlast && ok; ++tau) {
-        const int kb = tau == s0.x ? s0.y : 0, ke = tau == s1.x ? s1.y : nk;
-        const int rank = p.ranks[p.tiles[tau].x];
-        const uint32_t idesc = tc_idesc_bf16(TC_M, p.n * ((rank + 15) & ~15));
-        // the previous segment's accumulator has been drained
-        if (seg > 0 && !mbar_wait(acce, (seg - 1) & 1)) break;
-        tc_fence_after();
-        for (int k = kb; k < ke; ++k, ++g) {
-          const int s = g % NS;
-          if (!mbar_wait(&full[s], (g / NS) & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t xa = smem_u32(ring + s * STAGE), aa = xa + TC_XB;
-#pragma unroll
-          for (int kk = 0; kk < KW / 16; ++kk)
-            if ((int64_t)k * KW + kk * 16 < p.in)
-              tc_mma_bf16(tmem, tc_desc_sw128(xa + kk * 32), tc_desc_sw128(aa + kk * 32), idesc,
-                          (k > kb || kk > 0) ? 1u : 0u);
-          tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
+      for (int k = kb, g = 0; k < ke; ++k, ++g) {
+        const int s = g % NS;
+        if (!mbar_wait(&full[s], (g / NS) & 1)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        tc_commit(accf);
-        ++seg;
+        tc_fence_after();
+        const uint32_t xa = smem_u32(ring + s * STAGE), aa = xa + TC_XB;
+#pragma unroll
+        for (int kk = 0; kk < KW / 16; ++kk)
+          if ((int64_t)k * KW + kk * 16 < p.in)
+            tc_mma_bf16(tmem, tc_desc_sw128(xa + kk * 32), tc_desc_sw128(aa + kk * 32), idesc,
+                        (k > kb || kk > 0) ? 1u : 0u);
+        tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
       }
+      if (ok) tc_commit(accf);
       tc_commit(mdone);
       mbar_wait(mdone, 0);
     }
     __syncwarp();
-  } else if (any) {
+  } else if (any && warp >= 4 && warp < 8) {
     // ---------------------------------------------------------------- drain: one token row per thread
-    const int q = warp & 3, r = 32 * q + lane;
-    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
-    int seg = 0, nshared = 0;
-    bool ok = true;
-    for (int tau = s0.x; tau <= tlast && ok; ++tau) {
-      const int kb = tau == s0.x ? s0.y : 0, ke = tau == s1.x ? s1.y : nk;
-      const int4 td = p.tiles[tau];
-      const int slot = td.x, start = td.y, len = td.z;
-      const int rank = p.ranks[slot];
-      const int r16 = (rank + 15) & ~15, ncols = p.n * r16;
-      if (!(ok = wait_all(accf, seg & 1))) break;
-      tc_fence_after();
-      const bool whole = kb == 0 && ke == nk;
-      float *hrow = r < len ? p.h + (int64_t)p.perm[start + r] * p.ldh : nullptr;
-      // partial sums column-major, [slot][column][128 rows]: a warp writes 128 bytes a column
-      float *pcol = whole ? nullptr
-                          : p.part + (size_t)(2 * blockIdx.x + (tau == s0.x ? 0 : 1)) * p.sh_nc * TC_M + r;
+    const int r = 32 * (warp & 3) + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    // an empty share (more CTAs than stages) leaves zeros
+    const bool mine = ke > kb && has_k;
+    bool ok = !mine || wait_all(accf, 0);
+    if (ok) tc_fence_after();
+    if (ok && q > 0) {
+      // partial sums to this CTA's shared memory (the ring is no longer read), column-major
       for (int c0 = 0; c0 < ncols; c0 += 16) {
         float v[16];
-        if (has_k) {
+        if (mine) {
           tmem_ld16(trow + (uint32_t)c0, v);
         } else {
 #pragma unroll
           for (int e = 0; e < 16; ++e) v[e] = 0.f;
         }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) xbuf[(c0 + e) * TC_M + r] = v[e];
+      }
+      mbar_arrive_remote(xready, 0);                    // released to CTA 0
+      wait_all<true>(xdone, 0);                          // CTA 0 has read it
+    } else if (ok) {
+      if (cl > 1) ok = wait_all<true>(xready, 0);
+      float *hrow = r < len ? p.h + (int64_t)p.perm[start + r] * p.ldh : nullptr;
+      for (int c0 = 0; ok && c0 < ncols; c0 += 16) {
+        float v[16];
+        if (mine) {
+          tmem_ld16(trow + (uint32_t)c0, v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = 0.f;
+        }
+        // the other CTAs' partial sums, in cluster-rank order (16 loads in flight)
+        for (int qq = 1; qq < cl; ++qq) {
+          float u[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) u[e] = ld_dsmem_f1(&xbuf[(c0 + e) * TC_M + r], (uint32_t)qq);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] += u[e];
+        }
         const int i = c0 / r16, j0 = c0 - i * r16;
+        if (hrow) {
+          float *hp = hrow + (int64_t)i * p.R + j0;
+          if (j0 + 16 <= rank) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          if (j0 + e >= rank) v[e] = 0.f;   // columns past the rank come from padding rows of a
-        if (whole) {
-          if (hrow) {
-            float *hp = hrow + (int64_t)i * p.R + j0;
-            if (j0 + 16 <= rank) {
-#pragma unroll
-              for (int e = 0; e < 16; e += 4) *reinterpret_cast<float4 *>(hp + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; ++e)
-                if (j0 + e < rank) hp[e] = v[e];
-            }
-          }
-        } else if (r < len) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) pcol[(size_t)(c0 + e) * TC_M] = v[e];
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acce);   // the accumulator may be overwritten
-      ++seg;
-      if (whole) continue;
-      // a share of the tile: publish the partial sums (stages done, on the tile's ticket)
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pdone);
-      if (warp == 4 && lane == 0) {
-        if (mbar_wait(pdone, nshared & 1)) atomicAdd(&p.tickets[tau], ke - kb);
-      }
-      ++nshared;
-    }
-  }
-  // ------------------------------------------------------------------ final sums of shared tiles
-  // Every owner of a shared tile adds all owners' partial sums, in the owners'
-  // order, for its own slice of the tile's rows, once the tile's ticket shows all
-  // stages published.  Owners publish before they wait, so no wait depends on
-  // another.  All eight warps take part.
-  __syncthreads();
-  for (int pass = 0; any && pass < 2; ++pass) {
-    const int tau = pass == 0 ? s0.x : tlast;
-    if (pass == 1 && tlast == s0.x) break;
-    const int kb = tau == s0.x ? s0.y : 0, ke = tau == s1.x ? s1.y : nk;
-    if (kb == 0 && ke == nk) continue;           // a whole tile, already written
-    if (threadIdx.x == 0) {
-      int no = 0, me = 0;
-      const unsigned long long t0 = globaltimer();
-      for (uint32_t it = 0;; ++it) {
-        if (ld_acquire_gpu(&p.tickets[tau]) >= nk) break;
-        if ((it & 63u) == 63u && globaltimer() - t0 > kWaitLimitNs) {
-          flag_error(kErrWaitTimeout);
-          no = -1;
-          break;
-        }
-      }
-      if (no == 0) {
-        int bf = blockIdx.x;   // the owners are consecutive CTAs from the owner of the first stage
-        while (bf > 0 && before(make_int2(tau, 0), p.starts[bf])) --bf;
-        for (int b = bf;; ++b) {
-          const int2 sb = p.starts[b];
-          if (b > bf && sb.x != tau) break;            // past the tile's last owner
-          if (!before(sb, p.starts[b + 1])) continue;  // an empty share
-          if (no == TC_MAX_OWNERS) {
-            flag_error(kErrInternal);
-            no = -1;
-            break;
-          }
-          if (b == (int)blockIdx.x) me = no;
-          owners[no++] = 2 * b + (sb.x == tau ? 0 : 1);
-        }
-      }
-      last_flag[0] = no;
-      last_flag[1] = me;
-    }
-    __syncthreads();
-    const int no = last_flag[0], me = last_flag[1];
-    if (no > 0) {
-      const int4 td = p.tiles[tau];
-      const int start = td.y, len = td.z;
-      const int rank = p.ranks[td.x];
-      const int r16 = (rank + 15) & ~15, nq = p.n * r16 / 4;
-      const int r_lo = (int)((int64_t)len * me / no), r_hi = (int)((int64_t)len * (me + 1) / no);
-      const int nrows = r_hi - r_lo, nitems = nrows * nq;
-      // an item is 4 columns of one row, rows fastest (coalesced reads of the
-      // column-major partial sums); 4 items x 4 owners of loads in flight
-      for (int base = 0; base < nitems; base += TC_THREADS * 4) {
-        float acc[4][4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-        for (int o0 = 0; o0 < no; o0 += 4) {
-          float u[4][4][4];
-#pragma unroll
-          for (int oo = 0; oo < 4; ++oo)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int item = base + j * TC_THREADS + threadIdx.x;
-              const bool live = o0 + oo < no && item < nitems;
-              const int row = r_lo + (live ? item % nrows : 0), c = live ? 4 * (item / nrows) : 0;
-              const float *pc = p.part + ((size_t)owners[live ? o0 + oo : 0] * p.sh_nc + c) * TC_M + row;
-#pragma unroll
-              for (int e = 0; e < 4; ++e) u[oo][j][e] = live ? __ldcg(pc + (size_t)e * TC_M) : 0.f;
-            }
-#pragma unroll
-          for (int oo = 0; oo < 4; ++oo)
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) acc[j][e] += u[oo][j][e];
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int item = base + j * TC_THREADS + threadIdx.x;
-          if (item >= nitems) continue;
-          const int row = r_lo + item % nrows, c = 4 * (item / nrows);
-          const int i = c / r16, jj = c - i * r16;
-          float *hp = p.h + (int64_t)p.perm[start + row] * p.ldh + (int64_t)i * p.R + jj;
-          if (jj + 4 <= rank) {
-            *reinterpret_cast<float4 *>(hp) = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+            for (int e = 0; e < 16; e += 4)
+              *reinterpret_cast<float4 *>(hp + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
           } else {
+            // columns past the rank come from padding rows of a
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (jj + e < rank) hp[e] = acc[j][e];
+            for (int e = 0; e < 16; ++e)
+              if (j0 + e < rank) hp[e] = v[e];
           }
         }
       }
+      for (int qq = 1; qq < cl; ++qq) mbar_arrive_remote(xdone, (uint32_t)qq);
     }
-    __syncthreads();
   }
   pdl_launch_dependents();
   // every MMA has completed (the issuer waited for its last commit): free the tensor memory
@@ -1020,24 +828,6 @@ size_t sched_bytes(int64_t T, int S) {
 // h of apply_linear, kept between its two kernels (n * R <= kMaxHC columns)
 size_t hbuf_bytes(int64_t T, int R) { return ws_round((size_t)T * std::min(kMaxHC, LORA_MAX_SLICES * R) * 4); }
 
-// The shrink's split of work: CTA starts, per-tile tickets, partial sums of shared tiles.
-struct ShrinkWs {
-  int2 *starts;
-  int *tickets;
-  float *part;
-};
-int shrink_nc_bound(int R) { return (int)std::min<int64_t>(kMaxHC, (int64_t)LORA_MAX_SLICES * round_up(R, 16)); }
-size_t shrink_ws_bytes(int64_t T, int S, int R) {
-  return ws_round((size_t)(SH_MAX_CTAS + 1) * 8) + ws_round((size_t)max_tiles(T, S) * 4) +
-         ws_round((size_t)2 * SH_MAX_CTAS * TC_M * shrink_nc_bound(R) * 4);
-}
-bool carve_shrink(WsCarver &c, int64_t T, int S, int R, ShrinkWs &sw) {
-  sw.starts = (int2 *)c.take((size_t)(SH_MAX_CTAS + 1) * 8);
-  sw.tickets = (int *)c.take((size_t)max_tiles(T, S) * 4);
-  sw.part = (float *)c.take((size_t)2 * SH_MAX_CTAS * TC_M * shrink_nc_bound(R) * 4);
-  return sw.starts && sw.tickets && sw.part;
-}
-
 bool carve_sched(WsCarver &c, int64_t T, int S, SchedPtrs &sp) {
   sp.header = (int *)c.take(256);
   sp.counts = (int *)c.take((size_t)S * 4);
@@ -1047,15 +837,14 @@ bool carve_sched(WsCarver &c, int64_t T, int S, SchedPtrs &sp) {
 }
 
 lora_status_t launch_group(const lora_addressing_t &ad, const int32_t *ranks, int32_t *counts, int32_t *perm,
-                           int32_t *num_active, int *header, int4 *tiles, cudaStream_t st,
-                           SplitOut so = SplitOut{nullptr, nullptr, 0, 0, 0, 0, 0}) {
+                           int32_t *num_active, int *header, int4 *tiles, cudaStream_t st) {
   const int S = ad.num_slots;
-  int nw = (int)std::max<int64_t>(1, (160 * 1024 / 4 - 256 - 3 * S) / S);   // shared-memory bound
+  int nw = (int)std::max<int64_t>(1, (160 * 1024 / 4 - 256 - S) / S);   // shared-memory bound
   nw = std::min<int64_t>({nw, 32, std::max<int64_t>(1, ceil_div(ad.num_tokens, LORA_GROUP_TOKENS_PER_WARP))});
-  const size_t smem = (size_t)(nw * S + 3 * S + 161) * 4;
+  const size_t smem = (size_t)(nw * S + S + 160) * 4;
   LORA_CUDA(ensure_smem((const void *)group_kernel, smem));
   LORA_CUDA(launch(group_kernel, dim3(1), dim3(nw * 32), smem, st, 1, true, ad.slots, ad.num_tokens, S,
-                   ad.max_rank, ranks, counts, perm, num_active, header, tiles, (int)TC_M, so));
+                   ad.max_rank, ranks, counts, perm, num_active, header, tiles, (int)TC_M));
   return LORA_OK;
 }
 
@@ -1092,18 +881,13 @@ bool map_gather_rows(CUtensorMap *m, const void *base, int64_t rows, int64_t col
   return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Cost of a stage in the work split: n * rank16 adapter rows plus this weight for
-// the tile's x rows (128-byte rows).
-#ifndef LORA_SHRINK_XW
-#define LORA_SHRINK_XW TC_M
+// Cluster size of the shrink (CTAs splitting a tile's contraction); 0 picks one
+// from the tile bound so that the clusters about cover the SMs once.
+#ifndef LORA_SHRINK_CL
+#define LORA_SHRINK_CL 0
 #endif
 
-int shrink_grid() {
-  const int occ = occupancy((const void *)shrink_kernel, TC_THREADS, TC_BYTES);
-  return (int)std::min<int64_t>(SH_MAX_CTAS, std::max<int64_t>(1, (int64_t)occ * num_sms()));
-}
-
-lora_status_t launch_shrink(MArgs a, int64_t T, int G, cudaStream_t st) {
+lora_status_t launch_shrink(MArgs a, int64_t T, cudaStream_t st) {
   LORA_CUDA(ensure_smem((const void *)shrink_kernel, TC_BYTES));
   CUtensorMap tmX, tmXd, tmA16, tmA32, tmA64;
   memset(&tmX, 0, sizeof(tmX));
@@ -1113,12 +897,22 @@ lora_status_t launch_shrink(MArgs a, int64_t T, int G, cudaStream_t st) {
   memset(&tmA64, 0, sizeof(tmA64));
   a.T = (int)T;
   const int nc = a.n * (int)round_up(a.R, 16);   // most columns a slot can have
-  a.sh_nc = nc;
   a.tc_cols = 32;
   while (a.tc_cols < nc) a.tc_cols *= 2;
   a.sh_stage = TC_XB + nc * KW * 2;
   a.sh_ns = std::min(16, TC_RING / a.sh_stage);
-  if (a.sh_ns < 2 || nc > shrink_nc_bound(a.R) || a.tc_cols > 512) return LORA_ERR_UNSUPPORTED;
+  if (a.sh_ns < 2 || nc > kMaxHC || a.tc_cols > 512) return LORA_ERR_UNSUPPORTED;
+  a.nk = (int)std::max<int64_t>(1, ceil_div(a.in, KW));
+  const int64_t tiles = max_tiles(T, a.S);
+  int cl = LORA_SHRINK_CL;
+  if (cl <= 0) {
+    // about ceil(T / 128) + S / 2 tiles are real; cover the SMs once
+    const int64_t est = ceil_div(T, TC_M) + std::min<int64_t>(a.S, T) / 2, sms = num_sms();
+    cl = 1;
+    while (cl < 8 && est * cl * 2 * 4 <= sms * 5) cl *= 2;
+  }
+  while (cl > 1 && a.nk < cl) cl /= 2;
+  a.cl = cl;
   if (a.in > 0) {
     // one adapter when the slot stride is zero: a map over one slot, slot coordinate 0
     a.a_one_slot = a.sa_slot == 0 ? 1 : 0;
@@ -1130,8 +924,8 @@ lora_status_t launch_shrink(MArgs a, int64_t T, int G, cudaStream_t st) {
         !map_adapter(&tmA64, a.a, aS, arows, a.in, sslot, a.sa_row, 64))
       return LORA_ERR_ALIGNMENT;
   }
-  LORA_CUDA(launch(shrink_kernel, dim3((unsigned)G), dim3(TC_THREADS), TC_BYTES, st, 1, true, tmX, tmXd, tmA16,
-                   tmA32, tmA64, a));
+  LORA_CUDA(launch(shrink_kernel, dim3((unsigned)(tiles * cl)), dim3(TC_THREADS), TC_BYTES, st, cl, true, tmX,
+                   tmXd, tmA16, tmA32, tmA64, a));
   return LORA_OK;
 }
 
@@ -1215,33 +1009,20 @@ MArgs margs(const MultiArgs &m, const SchedPtrs &sp) {
   return a;
 }
 
-lora_status_t schedule(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, cudaStream_t st,
-                       SplitOut so = SplitOut{nullptr, nullptr, 0, 0, 0, 0, 0}) {
+lora_status_t schedule(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, cudaStream_t st) {
   if (!carve_sched(c, m.addr.num_tokens, m.addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
-  return launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st, so);
+  return launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st);
 }
 
-// Schedule plus the shrink's work split, then the shrink itself (h written to a.h).
+// Schedule, then the shrink itself (h written to `h`).
 lora_status_t schedule_and_shrink(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, MArgs *out, float *h,
                                   int64_t ldh, cudaStream_t st) {
-  const int64_t T = m.addr.num_tokens;
-  const int S = m.addr.num_slots, R = m.addr.max_rank;
-  if (!carve_sched(c, T, S, sp)) return LORA_ERR_WORKSPACE;
-  ShrinkWs sw;
-  if (!carve_shrink(c, T, S, R, sw)) return LORA_ERR_WORKSPACE;
-  const int G = shrink_grid();
-  const int nk = (int)std::max<int64_t>(1, ceil_div(m.in, KW));
-  SplitOut so{sw.starts, sw.tickets, G, m.n, nk, max_tiles(T, S), LORA_SHRINK_XW};
-  LORA_TRY(launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st, so));
+  LORA_TRY(schedule(m, c, sp, st));
   MArgs a = margs(m, sp);
   a.h = h;
   a.ldh = ldh;
-  a.starts = sw.starts;
-  a.tickets = sw.tickets;
-  a.part = sw.part;
-  a.nk = nk;
   *out = a;
-  return launch_shrink(a, T, G, st);
+  return launch_shrink(a, m.addr.num_tokens, st);
 }
 
 }  // namespace
@@ -1251,8 +1032,8 @@ size_t multi_ws_bytes(int op, int64_t T, int64_t in, int64_t O, int R, int S) {
   (void)O;
   if (T <= 0) return 0;
   if (op == LORA_OP_GROUP_BY_SLOT || op == LORA_OP_EXPAND) return sched_bytes(T, S);
-  if (op == LORA_OP_SHRINK) return sched_bytes(T, S) + shrink_ws_bytes(T, S, R);
-  if (op == LORA_OP_APPLY_LINEAR) return sched_bytes(T, S) + hbuf_bytes(T, R) + shrink_ws_bytes(T, S, R);
+  if (op == LORA_OP_SHRINK) return sched_bytes(T, S);
+  if (op == LORA_OP_APPLY_LINEAR) return sched_bytes(T, S) + hbuf_bytes(T, R);
   return 0;
 }
 
