@@ -120,6 +120,14 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 
 }  // namespace
 
+// Lanes holding the same key (a warp-wide match; the common case where all 32
+// lanes agree is checked first with one vote).
+__device__ __forceinline__ unsigned same_key_lanes(int key) {
+  const int k0 = __shfl_sync(0xffffffffu, key, 0);
+  if (__all_sync(0xffffffffu, key == k0)) return 0xffffffffu;
+  return __match_any_sync(0xffffffffu, key);
+}
+
 // =============================================================================
 // group_by_slot: one CTA.  Each warp owns a contiguous range of tokens; pass 1
 // counts active tokens per (warp, slot) (warp-level __match_any_sync, no
@@ -188,7 +196,9 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
   const int nw = blockDim.x >> 5;
   int *hist = gsm;                 // [nw][S]
   int *srank = gsm + nw * S;       // [S]
-  int *sh = srank + S;             // scan scratch (160 ints)
+  int *scnt = srank + S;           // [S] active tokens of each slot
+  int *sbase = scnt + S;           // [S] first position of each slot in the permutation
+  int *sh = sbase + S;             // scan scratch (160 ints)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
   const int t_lo = (int)((int64_t)T * warp / nw), t_hi = (int)((int64_t)T * (warp + 1) / nw);
@@ -214,31 +224,39 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
     }
 #pragma unroll
     for (int u = 0; u < GU; ++u) {
+      // inactive lanes share one class (fewer distinct values: a faster match)
       const bool act = active(sv[u]);
-      const unsigned m = __match_any_sync(0xffffffffu, act ? sv[u] : -(lane + 1));
+      const unsigned m = same_key_lanes(act ? sv[u] : -1);
       if (act && (m & lt) == 0) hist[warp * S + sv[u]] += __popc(m);
       __syncwarp();
     }
   }
   __syncthreads();
+  // per slot, a warp scans the warps' counts (lane w: warp w): hist becomes each
+  // warp's offset inside the slot, scnt the slot's total
+  for (int s = warp; s < S; s += nw) {
+    const int v = lane < nw ? hist[lane * S + s] : 0;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += n;
+    }
+    if (lane < nw) hist[lane * S + s] = inc - v;
+    if (lane == 31) scnt[s] = inc;
+  }
+  __syncthreads();
   int run = 0, trun = 0;
   for (int c0 = 0; c0 < S; c0 += blockDim.x) {
     const int s = c0 + threadIdx.x;
-    int cnt = 0;
-    if (s < S)
-      for (int w = 0; w < nw; ++w) cnt += hist[w * S + s];
+    const int cnt = s < S ? scnt[s] : 0;
     const int nt = (cnt + bmt - 1) / bmt;
     int ec, et, tc, tt;
     block_scan2(cnt, nt, ec, et, tc, tt, sh);
     if (s < S) {
       const int base = run + ec, tb = trun + et;
       counts_out[s] = cnt;
-      int cur = base;
-      for (int w = 0; w < nw; ++w) {
-        const int hcount = hist[w * S + s];
-        hist[w * S + s] = cur;
-        cur += hcount;
-      }
+      sbase[s] = base;
       for (int i = 0; i < nt; ++i) tiles[tb + i] = make_int4(s, base + i * bmt, min(bmt, cnt - i * bmt), 0);
     }
     run += tc;
@@ -262,13 +280,13 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
     for (int u = 0; u < GU; ++u) {
       const int t = t0 + u * 32 + lane;
       const bool act = active(sv[u]);
-      const unsigned m = __match_any_sync(0xffffffffu, act ? sv[u] : -(lane + 1));
+      const unsigned m = same_key_lanes(act ? sv[u] : -1);
       int cur = 0;
-      if (act) cur = hist[warp * S + sv[u]];
+      if (act) cur = sbase[sv[u]] + hist[warp * S + sv[u]];
       __syncwarp();
       if (act) {
         perm_out[cur + __popc(m & lt)] = t;
-        if ((m & lt) == 0) hist[warp * S + sv[u]] = cur + __popc(m);
+        if ((m & lt) == 0) hist[warp * S + sv[u]] = cur - sbase[sv[u]] + __popc(m);
       }
       __syncwarp();
     }
@@ -839,9 +857,9 @@ bool carve_sched(WsCarver &c, int64_t T, int S, SchedPtrs &sp) {
 lora_status_t launch_group(const lora_addressing_t &ad, const int32_t *ranks, int32_t *counts, int32_t *perm,
                            int32_t *num_active, int *header, int4 *tiles, cudaStream_t st) {
   const int S = ad.num_slots;
-  int nw = (int)std::max<int64_t>(1, (160 * 1024 / 4 - 256 - S) / S);   // shared-memory bound
+  int nw = (int)std::max<int64_t>(1, (160 * 1024 / 4 - 256 - 3 * S) / S);   // shared-memory bound
   nw = std::min<int64_t>({nw, 32, std::max<int64_t>(1, ceil_div(ad.num_tokens, LORA_GROUP_TOKENS_PER_WARP))});
-  const size_t smem = (size_t)(nw * S + S + 160) * 4;
+  const size_t smem = (size_t)(nw * S + 3 * S + 160) * 4;
   LORA_CUDA(ensure_smem((const void *)group_kernel, smem));
   LORA_CUDA(launch(group_kernel, dim3(1), dim3(nw * 32), smem, st, 1, true, ad.slots, ad.num_tokens, S,
                    ad.max_rank, ranks, counts, perm, num_active, header, tiles, (int)TC_M));
