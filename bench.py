@@ -4,7 +4,8 @@
 Workload: one batch of 8192 tokens x 4096 features in bf16 (the q_proj
 configuration: batch 4 x seq 2048, r = 16, scale 2) pushed through every step
 of the hot path, each through the C ABI of liblora.so:
-  training   lora_forward, lora_backward_dx_da, lora_backward_db (r = 16)
+  training   lora_forward_h (the forward, saving h = X A) and lora_backward
+             (dX, dA, dB in one call from the saved h), r = 16
   serving    lora_shrink, lora_expand, lora_apply_linear on the same batch as a
              fused QKV target (out_slices [4096, 1024, 1024], 32 adapter slots,
              R = 64, ranks from {0, 8, 16, 32, 64}, contiguous segments of
@@ -141,16 +142,18 @@ def build_single(torch, synth, dev, k):
     w["dX"] = torch.empty_like(w["X"])
     w["dA"] = torch.empty((K, r), dtype=torch.float32, device=dev)
     w["dB"] = torch.empty((r, L), dtype=torch.float32, device=dev)
+    w["h"] = torch.empty((M, r), dtype=torch.float32, device=dev)
     w["s"] = spec["s"]
     return w
 
 
 def single_bytes(M, K, L, r):
+    """What must cross HBM once: the forward reads X, A, B and reads and writes Y,
+    writing h; the backward reads X, dY, A, B and h and writes dX, dA, dB."""
     e = 2
     return {
-        "lora_forward": M * K * e + 2 * M * L * e + K * r * e + r * L * e,
-        "lora_backward_dx_da": M * L * e + 2 * M * K * e + K * r * e + r * L * e + K * r * 4,
-        "lora_backward_db": M * K * e + M * L * e + K * r * e + r * L * 4,
+        "lora_forward_h": M * K * e + 2 * M * L * e + K * r * e + r * L * e + M * r * 4,
+        "lora_backward": M * L * e + 2 * M * K * e + K * r * e + r * L * e + M * r * 4 + K * r * 4 + r * L * 4,
     }
 
 
@@ -196,7 +199,7 @@ def make_ops(torch, lora, binding, synth, dev):
         M, K = w["X"].shape
         r, L = w["B"].shape
         ws = {op: binding.workspace(op, binding.LORA_BF16, M, K, L, r, device=dev)
-              for op in (binding.OP_FORWARD, binding.OP_BACKWARD_DX_DA, binding.OP_BACKWARD_DB)}
+              for op in (binding.OP_FORWARD, binding.OP_BACKWARD)}
         mw = build_multi(torch, synth, dev, k, w["X"])
         O = sum(mw["out_slices"])
         for op in (binding.OP_SHRINK, binding.OP_EXPAND, binding.OP_APPLY_LINEAR):
@@ -216,16 +219,12 @@ def make_ops(torch, lora, binding, synth, dev):
 
     def fwd(S):
         w = S["w"]
-        lora.lora_forward(w["X"], w["A"], w["B"], w["Y"], w["s"], ws=S["ws"][binding.OP_FORWARD])
+        lora.lora_forward_h(w["X"], w["A"], w["B"], w["Y"], w["s"], w["h"], ws=S["ws"][binding.OP_FORWARD])
 
-    def dxda(S):
+    def bwd(S):
         w = S["w"]
-        lora.lora_backward_dx_da(w["X"], w["dY"], w["A"], w["B"], w["s"], w["dX"], w["dA"],
-                                 ws=S["ws"][binding.OP_BACKWARD_DX_DA])
-
-    def db(S):
-        w = S["w"]
-        lora.lora_backward_db(w["X"], w["A"], w["dY"], w["s"], w["dB"], ws=S["ws"][binding.OP_BACKWARD_DB])
+        lora.lora_backward(w["X"], w["dY"], w["A"], w["B"], w["h"], w["s"], w["dX"], w["dA"], w["dB"],
+                           ws=S["ws"][binding.OP_BACKWARD])
 
     def shrink(S):
         m = S["mw"]
@@ -245,9 +244,8 @@ def make_ops(torch, lora, binding, synth, dev):
     def gather(S):
         lora.lora_gather_shrink(gids, ga, gslots, granks, gw["R"], gw["hg"])
 
-    ops = [("lora_forward", fwd, by["lora_forward"]),
-           ("lora_backward_dx_da", dxda, by["lora_backward_dx_da"]),
-           ("lora_backward_db", db, by["lora_backward_db"]),
+    ops = [("lora_forward_h", fwd, by["lora_forward_h"]),
+           ("lora_backward", bwd, by["lora_backward"]),
            ("lora_shrink", shrink, by["lora_shrink"]),
            ("lora_expand", expand, by["lora_expand"]),
            ("lora_apply_linear", apply, by["lora_apply_linear"]),

@@ -82,7 +82,8 @@ typedef enum {
     LORA_OP_SHRINK = 4,
     LORA_OP_EXPAND = 5,
     LORA_OP_APPLY_LINEAR = 6,
-    LORA_OP_GATHER_SHRINK = 7
+    LORA_OP_GATHER_SHRINK = 7,
+    LORA_OP_BACKWARD = 8
 } lora_op_t;
 
 /* Token -> adapter-slot addressing of the multi-adapter ops ([mstar lora.ops]
@@ -124,6 +125,44 @@ LORA_API lora_status_t lora_forward(lora_dtype_t dtype, int64_t M, int64_t K, in
                            const void *B, int64_t sB_r, int64_t sB_l,
                            void *Y, int64_t ldy, float scale,
                            void *ws, size_t ws_bytes, void *stream);
+
+/* --------------------------------------------------------------------------------
+ * lora_forward_h:  lora_forward, and also h = X * A (the rank-r hidden rows the
+ * forward computes on the way, [NeMo lora_kernel] inner_kernel) written out for
+ * lora_backward, which then needs neither X * A again nor a second read of X.
+ *   h     float32 [M][ldh] (caller-owned device memory, ldh >= r), overwritten.
+ *   ws:   lora_workspace_size(LORA_OP_FORWARD, ...) bytes, as for lora_forward.
+ * Errors as lora_forward; h == NULL or ldh < r -> LORA_ERR_INVALID_ARG.
+ * -------------------------------------------------------------------------------- */
+LORA_API lora_status_t lora_forward_h(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r,
+                           const void *X, int64_t ldx,
+                           const void *A, int64_t sA_k, int64_t sA_r,
+                           const void *B, int64_t sB_r, int64_t sB_l,
+                           void *Y, int64_t ldy, float scale,
+                           float *h, int64_t ldh,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* --------------------------------------------------------------------------------
+ * lora_backward:  dX, dA and dB in one call from the h that lora_forward_h saved:
+ *   dyb = dY*B^T;  dX = scale * dyb*A^T;  dA = scale * X^T*dyb;  dB = scale * h^T*dY
+ * [NeMo lora_kernel] lora_da_dx_kernel / lora_da_dx_update_wrapper (dX, dA) and
+ * lora_db_kernel / lora_db_update_wrapper (dB, whose X * A is the saved h),
+ * restated in the forward roles.  X is read once (by the dX / dA pass).
+ *   X, dY, A, B, dX, dA as in lora_backward_dx_da;  dB as in lora_backward_db.
+ *   h     float32 [M][ldh], ldh >= r: X * A as lora_forward_h wrote it.
+ *   ws:   lora_workspace_size(LORA_OP_BACKWARD, ...) bytes.
+ * dX, dA and dB are overwritten.  Errors as lora_backward_dx_da and
+ * lora_backward_db; h == NULL or ldh < r -> LORA_ERR_INVALID_ARG.
+ * -------------------------------------------------------------------------------- */
+LORA_API lora_status_t lora_backward(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r,
+                          const void *X, int64_t ldx, const void *dY, int64_t lddy,
+                          const void *A, int64_t sA_k, int64_t sA_r,
+                          const void *B, int64_t sB_r, int64_t sB_l,
+                          const float *h, int64_t ldh, float scale,
+                          void *dX, int64_t lddx,
+                          float *dA, int64_t sdA_k, int64_t sdA_r,
+                          float *dB, int64_t sdB_r, int64_t sdB_l,
+                          void *ws, size_t ws_bytes, void *stream);
 
 /* --------------------------------------------------------------------------------
  * lora_backward_dx_da:  dyb = dY*B^T;  dX = scale * dyb*A^T;  dA = scale * X^T*dyb

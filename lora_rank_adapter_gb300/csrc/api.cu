@@ -136,7 +136,7 @@ static size_t single_ws_needed(int op, const SingleArgs &a) {
   if (a.dtype != LORA_BF16) return f32_ws_bytes(op, a.M, a.K, a.L, a.r);
   size_t full = bf16_ws_bytes(op, a.M, a.K, a.L, a.r);
   if (op == LORA_OP_FORWARD) {
-    SingleLayout lay = plan_layout(a, true, true);
+    SingleLayout lay = plan_layout(a, true, a.L > 0);
     size_t n = 0;
     if (lay.pack_A) n += ws_round((size_t)a.r * round_up(a.K, 8) * 2);
     if (lay.pack_B) n += ws_round((size_t)a.L * round_up(a.r, 8) * 2);
@@ -174,6 +174,7 @@ size_t lora_workspace_size(lora_op_t op, lora_dtype_t dtype, int64_t m_or_t, int
     case LORA_OP_FORWARD:
     case LORA_OP_BACKWARD_DX_DA:
     case LORA_OP_BACKWARD_DB:
+    case LORA_OP_BACKWARD:
       if (!size_ok(m_or_t) || !size_ok(k_or_in) || !size_ok(l_or_o) || r_or_R < 0 || r_or_R > LORA_MAX_RANK)
         return 0;
       return single_ws(op, dtype, m_or_t, k_or_in, l_or_o, r_or_R);
@@ -207,6 +208,59 @@ lora_status_t lora_forward(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, 
   LORA_TRY(check_ws(ws, ws_bytes, single_ws_needed(LORA_OP_FORWARD, a)));
   cudaStream_t st = (cudaStream_t)stream;
   return dtype == LORA_BF16 ? forward_bf16(a, ws, ws_bytes, st) : forward_f32(a, st);
+}
+
+lora_status_t lora_forward_h(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r, const void *X,
+                             int64_t ldx, const void *A, int64_t sA_k, int64_t sA_r, const void *B, int64_t sB_r,
+                             int64_t sB_l, void *Y, int64_t ldy, float scale, float *h, int64_t ldh, void *ws,
+                             size_t ws_bytes, void *stream) {
+  LORA_TRY(check_single_common(dtype, M, K, L, r));
+  if (M > 0 && r > 0 && (h == nullptr || ldh < r)) return LORA_ERR_INVALID_ARG;
+  const int e = dtype == LORA_BF16 ? 2 : 4;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (M == 0 || r == 0) return LORA_OK;
+  if (K == 0) return fill_zero_2d(LORA_F32, h, M, r, ldh, 1, st);   // h = X * A = 0 and Y += 0
+  LORA_TRY(check_big(X, M, K, ldx, e));
+  LORA_TRY(check_big(Y, M, L, ldy, e));
+  if (A == nullptr || (L > 0 && B == nullptr)) return LORA_ERR_INVALID_ARG;
+  SingleArgs a{};
+  a.dtype = dtype; a.M = M; a.K = K; a.L = L; a.r = r;
+  a.X = X; a.ldx = ldx; a.A = A; a.sA_k = sA_k; a.sA_r = sA_r; a.B = B; a.sB_r = sB_r; a.sB_l = sB_l;
+  a.Y = Y; a.ldy = ldy; a.scale = scale; a.h = h; a.ldh = ldh;
+  LORA_TRY(check_ws(ws, ws_bytes, single_ws_needed(LORA_OP_FORWARD, a)));
+  return dtype == LORA_BF16 ? forward_bf16(a, ws, ws_bytes, st) : forward_f32(a, st);
+}
+
+lora_status_t lora_backward(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r, const void *X, int64_t ldx,
+                            const void *dY, int64_t lddy, const void *A, int64_t sA_k, int64_t sA_r, const void *B,
+                            int64_t sB_r, int64_t sB_l, const float *h, int64_t ldh, float scale, void *dX,
+                            int64_t lddx, float *dA, int64_t sdA_k, int64_t sdA_r, float *dB, int64_t sdB_r,
+                            int64_t sdB_l, void *ws, size_t ws_bytes, void *stream) {
+  LORA_TRY(check_single_common(dtype, M, K, L, r));
+  const int e = dtype == LORA_BF16 ? 2 : 4;
+  LORA_TRY(check_big(X, M, K, ldx, e));
+  LORA_TRY(check_big(dY, M, L, lddy, e));
+  LORA_TRY(check_big(dX, M, K, lddx, e));
+  if (K > 0 && r > 0 && dA == nullptr) return LORA_ERR_INVALID_ARG;
+  if (L > 0 && r > 0 && dB == nullptr) return LORA_ERR_INVALID_ARG;
+  if (M > 0 && r > 0 && (h == nullptr || ldh < r)) return LORA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (M == 0 || K == 0 || L == 0 || r == 0) {
+    // an empty sum somewhere: the calls that handle it compute what is left
+    LORA_TRY(lora_backward_dx_da(dtype, M, K, L, r, X, ldx, dY, lddy, A, sA_k, sA_r, B, sB_r, sB_l, scale, dX, lddx,
+                                 dA, sdA_k, sdA_r, ws, ws_bytes, stream));
+    // dB is an empty sum (M == 0), empty (L or r == 0), or zero with h = X * A = 0 (K == 0)
+    return fill_zero_2d(LORA_F32, dB, r, L, sdB_r, sdB_l, st);
+  }
+  if (A == nullptr || B == nullptr) return LORA_ERR_INVALID_ARG;
+  SingleArgs a{};
+  a.dtype = dtype; a.M = M; a.K = K; a.L = L; a.r = r;
+  a.X = X; a.ldx = ldx; a.dY = dY; a.lddy = lddy; a.A = A; a.sA_k = sA_k; a.sA_r = sA_r;
+  a.B = B; a.sB_r = sB_r; a.sB_l = sB_l; a.scale = scale; a.dX = dX; a.lddx = lddx;
+  a.dA = dA; a.sdA_k = sdA_k; a.sdA_r = sdA_r; a.dB = dB; a.sdB_r = sdB_r; a.sdB_l = sdB_l;
+  a.h = const_cast<float *>(h); a.ldh = ldh;
+  LORA_TRY(check_ws(ws, ws_bytes, single_ws_needed(LORA_OP_BACKWARD, a)));
+  return dtype == LORA_BF16 ? backward_bf16(a, ws, ws_bytes, st) : backward_f32(a, ws, ws_bytes, st);
 }
 
 lora_status_t lora_backward_dx_da(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r, const void *X,

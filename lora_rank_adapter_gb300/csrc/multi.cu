@@ -813,15 +813,26 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t *__restrict__
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t t = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
-    const int s = slots[t];
+    // the slot and the id are independent loads: issue both before either is used
+    const int s = __ldg(&slots[t]);
+    const int64_t id = __ldg(&ids[t]);
     if (s < 0 || s >= S) continue;
-    const int rank = ranks[s];
+    const int rank = __ldg(&ranks[s]);
     if (rank < 1 || rank > R) continue;
-    const int64_t id = ids[t];
     const bool valid = id >= 0 && id < V;
     const __nv_bfloat16 *col = a + (int64_t)s * sa_slot + (valid ? id : 0) * sa_col;
-    for (int j = lane; j < rank; j += 32)
-      h[t * ldh + j] = valid ? __bfloat162float(col[(int64_t)j * sa_row]) : 0.f;
+    // up to 4 rank entries per lane, all loads in flight before the stores
+    float v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = lane + 32 * q;
+      v[q] = valid && j < rank ? __bfloat162float(col[(int64_t)j * sa_row]) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = lane + 32 * q;
+      if (j < rank) h[t * ldh + j] = v[q];
+    }
   }
   pdl_launch_dependents();
 }

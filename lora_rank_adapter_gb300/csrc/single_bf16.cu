@@ -303,6 +303,21 @@ __global__ void __launch_bounds__(NTHREADS_LS) fwd_bf16_kernel(const __grid_cons
       if (c != (int)crank) mbar_arrive_remote(hdone, c);
   }
 
+  // the full h of this row block (identical in every CTA of the cluster): CTA 0 writes it out
+  if (ok && p.h != nullptr && crank == 0) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int64_t m = m0 + 16 * w + gq + 8 * hf;
+      if (m >= p.M) continue;
+      float *hrow = p.h + m * p.ldh;
+#pragma unroll
+      for (int nt = 0; nt < RP / 8; ++nt) {
+        const int j = nt * 8 + 2 * cq;
+        if (j < p.r) hrow[j] = hacc[nt][2 * hf];
+        if (j + 1 < p.r) hrow[j + 1] = hacc[nt][2 * hf + 1];
+      }
+    }
+  }
   // h as A fragments (hi + lo bf16)
   uint32_t ahi[RP / 16][4], alo[RP / 16][4];
 #pragma unroll
@@ -384,6 +399,31 @@ __device__ __forceinline__ void write_blob_rows(uint8_t *blob, int w, int gq, in
       *reinterpret_cast<uint32_t *>(bhi + o) = h;
       *reinterpret_cast<uint32_t *>(blo + o) = l;
     }
+}
+
+// The saved h (fp32 [M][ldh], columns j < r; zero past r and past M) as the
+// column pass's hi/lo blob, one 64-row block per CTA.  Block 0 also zeroes the
+// column-pass counters.
+template <int RP>
+__global__ void __launch_bounds__(256) hblob_kernel(const float *__restrict__ h, int64_t ldh, int64_t M, int r,
+                                                    uint8_t *blob, int *counters, int ncounters) {
+  pdl_wait();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < ncounters; i += blockDim.x) counters[i] = 0;
+  uint8_t *bhi = blob + (size_t)blockIdx.x * blob_bytes<RP>(), *blo = bhi + RP * 128;
+  const int64_t m0 = (int64_t)blockIdx.x * BM;
+  for (int e = threadIdx.x; e < BM * RP / 2; e += blockDim.x) {
+    const int row = e / (RP / 2), col = 2 * (e % (RP / 2));
+    const int64_t m = m0 + row;
+    const float v0 = m < M && col < r ? h[m * ldh + col] : 0.f;
+    const float v1 = m < M && col + 1 < r ? h[m * ldh + col + 1] : 0.f;
+    uint32_t hi, lo;
+    split_bf16(v0, v1, hi, lo);
+    const uint32_t o = lr_off<RP>(row, col);
+    *reinterpret_cast<uint32_t *>(bhi + o) = hi;
+    *reinterpret_cast<uint32_t *>(blo + o) = lo;
+  }
+  pdl_launch_dependents();
 }
 
 template <int RP, bool kW_KN>
@@ -926,6 +966,11 @@ size_t bf16_ws_bytes(int op, int64_t M, int64_t K, int64_t L, int r) {
     const int64_t nlb = ceil_div(L, 64);
     return packA + blob + ws_round((size_t)kMsplitMax * RP * nlb * 64 * 4) + ws_round((size_t)nlb * 4);
   }
+  if (op == LORA_OP_BACKWARD) {
+    const int64_t nlb = ceil_div(L, 64);
+    return bf16_ws_bytes(LORA_OP_BACKWARD_DX_DA, M, K, L, r) + blob +
+           ws_round((size_t)kMsplitMax * RP * nlb * 64 * 4) + ws_round((size_t)nlb * 4);
+  }
   return 0;
 }
 
@@ -963,14 +1008,19 @@ static lora_status_t pack_operands(const SingleArgs &a, const SingleLayout &lay,
 
 template <int RP>
 static lora_status_t forward_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st) {
-  SingleLayout lay = plan_layout(a, true, true);
+  SingleLayout lay = plan_layout(a, true, a.L > 0);
   WsCarver carver(ws, ws_bytes);
   const void *Ac = nullptr, *Bc = nullptr;
   LORA_TRY(pack_operands(a, lay, carver, &Ac, &Bc, st, true));
   CUtensorMap tX, tA, tB, tY;
-  if (!map_big(&tX, a.X, a.M, a.K, a.ldx) || !map_ac(&tA, Ac, a.K, a.r, lay.lda, RP) ||
-      !map_bc(&tB, Bc, a.L, a.r, lay.ldb, RP) || !map_big(&tY, a.Y, a.M, a.L, a.ldy))
+  if (!map_big(&tX, a.X, a.M, a.K, a.ldx) || !map_ac(&tA, Ac, a.K, a.r, lay.lda, RP)) return LORA_ERR_ALIGNMENT;
+  if (a.L == 0) {
+    // h only (lora_forward_h with no output columns): no Y or B tile is ever loaded
+    tB = tA;
+    tY = tX;
+  } else if (!map_bc(&tB, Bc, a.L, a.r, lay.ldb, RP) || !map_big(&tY, a.Y, a.M, a.L, a.ldy)) {
     return LORA_ERR_ALIGNMENT;
+  }
   auto kern = fwd_bf16_kernel<RP>;
   const size_t smem = FwdCfg<RP>::BYTES;
   LORA_CUDA(ensure_smem((const void *)kern, smem));
@@ -979,7 +1029,7 @@ static lora_status_t forward_rp(const SingleArgs &a, void *ws, size_t ws_bytes, 
   const int64_t nk = ceil_div(a.K, BK), nl = ceil_div(a.L, BK);
   int cl = pick_pow2(nrb, (int64_t)occ * num_sms(), 8);
   while (cl > 1 && (nk < cl || nl < cl)) cl /= 2;
-  FwdArgs p{(int)a.M, (int)a.K, (int)a.L, a.scale, cl};
+  FwdArgs p{(int)a.M, (int)a.K, (int)a.L, a.scale, cl, a.h, a.ldh, a.r};
   LORA_CUDA(launch(kern, dim3((unsigned)(nrb * cl)), dim3(NTHREADS_LS), smem, st, cl, true, tX, tA, tB, tY, p));
   return LORA_OK;
 }
@@ -1069,6 +1119,10 @@ lora_status_t backward_dx_da_bf16(const SingleArgs &a, void *ws, size_t ws_bytes
 }
 
 template <int RP>
+static lora_status_t launch_colpass_db(const SingleArgs &a, const uint8_t *blob, float *partB, int *counters,
+                                       cudaStream_t st);
+
+template <int RP>
 static lora_status_t db_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st) {
   SingleLayout lay = plan_layout(a, true, false);
   WsCarver carver(ws, ws_bytes);
@@ -1082,7 +1136,14 @@ static lora_status_t db_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cudaS
   int *counters = (int *)carver.take((size_t)nlb * 4);
   if (!blob || !partB || !counters) return LORA_ERR_WORKSPACE;
   LORA_TRY((launch_rows<RP, false>(a.X, a.ldx, a.K, tA, a.M, blob, counters, (int)nlb, st)));
+  return launch_colpass_db<RP>(a, blob, partB, counters, st);
+}
 
+// dB = s * h^T * dY from the h blob (the column pass of lora_backward_db).
+template <int RP>
+static lora_status_t launch_colpass_db(const SingleArgs &a, const uint8_t *blob, float *partB, int *counters,
+                                       cudaStream_t st) {
+  const int64_t nlb = ceil_div(a.L, BK);
   auto kern = colpass_db_kernel<RP>;
   const size_t smem = DbCfg<RP>::BYTES;
   LORA_CUDA(ensure_smem((const void *)kern, smem));
@@ -1101,9 +1162,35 @@ static lora_status_t db_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cudaS
   p.out = a.dB;
   p.out_s0 = a.sdB_r;
   p.out_s1 = a.sdB_l;
-  p.blob = blob;
+  p.blob = const_cast<uint8_t *>(blob);
   LORA_CUDA(launch(kern, dim3((unsigned)(nlb * ms)), dim3(NTHREADS), smem, st, 1, true, tDY, p));
   return LORA_OK;
+}
+
+// lora_backward: the dX / dA passes of lora_backward_dx_da, then dB from the saved h.
+template <int RP>
+static lora_status_t backward_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st) {
+  const size_t n1 = bf16_ws_bytes(LORA_OP_BACKWARD_DX_DA, a.M, a.K, a.L, a.r);
+  if (ws_bytes < n1) return LORA_ERR_WORKSPACE;
+  LORA_TRY(dxda_rp<RP>(a, ws, n1, st));
+  WsCarver carver(static_cast<char *>(ws) + n1, ws_bytes - n1);
+  const int64_t nlb = ceil_div(a.L, BK), nrb = ceil_div(a.M, BM);
+  uint8_t *blob = (uint8_t *)carver.take((size_t)nrb * RP * 256);
+  float *partB = (float *)carver.take((size_t)kMsplitMax * RP * nlb * 64 * 4);
+  int *counters = (int *)carver.take((size_t)nlb * 4);
+  if (!blob || !partB || !counters) return LORA_ERR_WORKSPACE;
+  LORA_CUDA(launch(hblob_kernel<RP>, dim3((unsigned)nrb), dim3(256), 0, st, 1, true, (const float *)a.h, a.ldh, a.M,
+                   a.r, blob, counters, (int)nlb));
+  return launch_colpass_db<RP>(a, blob, partB, counters, st);
+}
+
+lora_status_t backward_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st) {
+  switch (rank_bucket(a.r)) {
+    case 16: return backward_rp<16>(a, ws, ws_bytes, st);
+    case 32: return backward_rp<32>(a, ws, ws_bytes, st);
+    case 64: return backward_rp<64>(a, ws, ws_bytes, st);
+    default: return backward_rp<128>(a, ws, ws_bytes, st);
+  }
 }
 
 lora_status_t backward_db_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st) {

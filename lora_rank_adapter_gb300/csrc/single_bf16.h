@@ -24,6 +24,7 @@ struct SingleArgs {
   float *dA; int64_t sdA_k, sdA_r;
   float *dB; int64_t sdB_r, sdB_l;
   float scale;
+  float *h; int64_t ldh;      // forward: optional h = X * A out; backward: the saved h in
 };
 
 // Whether A / B are repacked into the workspace, and the row strides used.
@@ -36,6 +37,9 @@ struct FwdArgs {
   int M, K, L;
   float scale;
   int cl;
+  float *h;        // optional: h = X * A, [M][ldh] fp32, columns j < r
+  int64_t ldh;
+  int r;
 };
 
 struct RowsArgs {
@@ -62,10 +66,12 @@ size_t f32_ws_bytes(int op, int64_t M, int64_t K, int64_t L, int r);
 lora_status_t forward_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
 lora_status_t backward_dx_da_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
 lora_status_t backward_db_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
+lora_status_t backward_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
 
 lora_status_t forward_f32(const SingleArgs &a, cudaStream_t st);
 lora_status_t backward_dx_da_f32(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
 lora_status_t backward_db_f32(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
+lora_status_t backward_f32(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
 
 // Zero fills used for degenerate shapes (outputs defined as overwritten).
 lora_status_t fill_zero_2d(lora_dtype_t dt, void *p, int64_t rows, int64_t cols, int64_t s_row, int64_t s_col,

@@ -36,7 +36,10 @@ __global__ void __launch_bounds__(256) fwd_f32_kernel(SingleArgs a) {
     if (m < a.M)
       for (int64_t k = lane; k < a.K; k += 32) acc += X[m * a.ldx + k] * A[k * a.sA_k + j * a.sA_r];
     acc = warp_sum(acc);
-    if (lane == 0) h[row * a.r + j] = acc;
+    if (lane == 0) {
+      h[row * a.r + j] = acc;
+      if (a.h != nullptr && m < a.M) a.h[m * a.ldh + j] = acc;   // lora_forward_h
+    }
   }
   __syncthreads();
   for (int row = 0; row < kF32Rows; ++row) {
@@ -132,7 +135,8 @@ size_t f32_ws_bytes(int op, int64_t M, int64_t K, int64_t L, int r) {
   (void)K;
   (void)L;
   if (M <= 0 || r <= 0) return 0;
-  if (op == LORA_OP_BACKWARD_DX_DA || op == LORA_OP_BACKWARD_DB) return ws_round((size_t)M * r * 4);
+  if (op == LORA_OP_BACKWARD_DX_DA || op == LORA_OP_BACKWARD_DB || op == LORA_OP_BACKWARD)
+    return ws_round((size_t)M * r * 4);
   return 0;
 }
 
@@ -167,6 +171,16 @@ lora_status_t backward_db_f32(const SingleArgs &a, void *ws, size_t ws_bytes, cu
   // dB(j, l) = s * sum_m h[m][j] * dY[m][l]
   LORA_CUDA(launch(coldot_f32_kernel, dim3(grid_for((int64_t)a.r * a.L, 8)), dim3(256), 0, st, 1, true,
                    (const float *)h, (int64_t)a.r, (int64_t)1, (int64_t)a.r, (const float *)a.dY, a.lddy, a.L, a.M,
+                   a.scale, a.dB, a.sdB_r, a.sdB_l));
+  return LORA_OK;
+}
+
+// lora_backward: dX and dA as lora_backward_dx_da, dB from the saved h.
+lora_status_t backward_f32(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st) {
+  LORA_TRY(backward_dx_da_f32(a, ws, ws_bytes, st));
+  // dB(j, l) = s * sum_m h[m][j] * dY[m][l]
+  LORA_CUDA(launch(coldot_f32_kernel, dim3(grid_for((int64_t)a.r * a.L, 8)), dim3(256), 0, st, 1, true,
+                   (const float *)a.h, a.ldh, (int64_t)1, (int64_t)a.r, (const float *)a.dY, a.lddy, a.L, a.M,
                    a.scale, a.dB, a.sdB_r, a.sdB_l));
   return LORA_OK;
 }

@@ -17,7 +17,7 @@ def L():
 
 def test_every_declared_symbol_is_exported(L):
     declared = header_functions()
-    assert len(declared) == 14, declared
+    assert len(declared) == 16, declared
     assert sorted(B.EXPORTS) == declared
     for name in declared:
         assert hasattr(L, name), name
@@ -82,8 +82,25 @@ def test_backward_argument_errors(L):
     assert db() == 4
 
 
+def test_fused_argument_errors(L):
+    fh = lambda **k: L.lora_forward_h(1, k.get("M", 64), 64, 64, 16, FAKE, 64, FAKE, 1, 64, FAKE, 1, 16, FAKE, 64,
+                                      1.0, k.get("h", FAKE), k.get("ldh", 16), NULL, 0, S0)
+    assert fh(h=NULL) == 1                         # h is required
+    assert fh(ldh=8) == 1                          # ldh < r
+    assert fh(M=0, h=NULL) == 0                    # nothing to write
+    bw = lambda **k: L.lora_backward(1, 64, 64, 64, 16, FAKE, 64, FAKE, 64, FAKE, 1, 64, FAKE, 1, 16,
+                                     k.get("h", FAKE), k.get("ldh", 16), 1.0, FAKE, 64, FAKE, 16, 1,
+                                     k.get("dB", FAKE), 64, 1, k.get("ws", NULL), k.get("wsb", 0), S0)
+    assert bw(h=NULL) == 1
+    assert bw(ldh=4) == 1
+    assert bw(dB=NULL) == 1
+    assert bw() == 4                               # needs workspace
+    need = L.lora_workspace_size(B.OP_BACKWARD, 1, 64, 64, 64, 16, 0)
+    assert need >= L.lora_workspace_size(B.OP_BACKWARD_DX_DA, 1, 64, 64, 64, 16, 0)
+
+
 def test_workspace_sizes_monotone(L):
-    for op in (B.OP_FORWARD, B.OP_BACKWARD_DX_DA, B.OP_BACKWARD_DB):
+    for op in (B.OP_FORWARD, B.OP_BACKWARD_DX_DA, B.OP_BACKWARD_DB, B.OP_BACKWARD):
         small = L.lora_workspace_size(op, 1, 256, 512, 512, 8, 0)
         big = L.lora_workspace_size(op, 1, 8192, 4096, 4096, 16, 0)
         assert big >= small >= 0
