@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const bool aw = warp >= TC_AW0 && warp < TC_AW0 + TC_AW;   // adapter loader
   if (any && (warp < TC_XW || aw)) {
     // ---------------------------------------------------------------- loader warps
-    const int par = aw ? warp - TC_AW0 : warp, nw = aw ? TC_AW : TC_XW;   // stages g % nw == par
+    const int par = aw ? warp - TC_AW0 : warp, nw = aw ? TC_AW : TC_XW;   // stages s % nw == par
     if (lane == 0 && has_k) {
       if (aw) {
         prefetch_tmap(&tmA16);
@@ -430,7 +430,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int aslot = p.a_one_slot ? 0 : slot;
     const uint32_t tx = has_k ? (uint32_t)(TC_XB + ncols * KW * 2) : 0u;
     for (int k = kb, g = 0; k < ke; ++k, ++g) {
-      if (g % nw != par) continue;              // another loader warp's stage
+      // a loader warp owns stages s with s % nw == par and takes all their uses in
+      // order, so its wait on a stage's empty barrier is always for the use just
+      // before (a later use could otherwise pass an earlier one of the same parity)
+      if ((g % NS) % nw != par) continue;
       const int s = g % NS;
       if (g >= NS && !wait_all(&empty[s], ((g / NS) & 1) ^ 1)) break;
       uint8_t *st = ring + s * STAGE;
