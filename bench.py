@@ -262,10 +262,11 @@ def h2d_d2h_tensors(S):
 
 
 # ----------------------------------------------------------------------------- oracle timing
-def oracle_sample_pass(O, synth, torch, tokens):
-    """One pass of the oracle over a `tokens`-row sample of the workload (every
-    op of the step; the gather over a 4096-entry axis, its cost per token does
-    not depend on the axis length)."""
+def oracle_sample(O, synth, torch, tokens):
+    """Inputs of a `tokens`-row sample of the workload, and a function that runs
+    every op of the step on them through the oracle and returns the seconds it
+    took (the gather over a 4096-entry axis: its cost per token does not depend
+    on the axis length)."""
     spec = synth.single_spec("single_c2", M=tokens)
     gen = "cuda" if torch.cuda.is_available() else "cpu"
     w = synth.make_single(spec, seed=SEED, device=gen, prefix="cpu")
@@ -276,32 +277,40 @@ def oracle_sample_pass(O, synth, torch, tokens):
     gs = synth.multi_spec("multi_c5", T=tokens, IN=64, out_slices=[64], S=32, V=4096)
     gw = synth.make_multi(gs, seed=SEED, device=gen)
     sl, rk, sc = (mw[k].cpu().numpy() for k in ("slots", "ranks", "scalings"))
+    sc = sc.astype(np.float64)
     a, b, y0 = f(mw["a"]), f(mw["b"]), f(mw["y0"])
     ga, gsl, grk, gid = f(gw["ga"]), gw["slots"].cpu().numpy(), gw["ranks"].cpu().numpy(), gw["ids"].cpu().numpy()
     R, osl = ms["R"], ms["out_slices"]
-    t0 = time.perf_counter()
-    O.forward(X, A, B, Y0, spec["s"])
-    O.backward_dx_da(X, dY, A, B, spec["s"])
-    O.backward_db(X, A, dY, spec["s"])
-    h = O.shrink(X, a, sl, rk, R, len(osl))
-    O.expand(h, b, sl, rk, sc.astype(np.float64), y0, osl, R)
-    O.apply_linear(X, a, b, sl, rk, sc.astype(np.float64), y0, osl, R)
-    O.gather_shrink(gid, ga, gsl, grk, gs["R"])
-    return time.perf_counter() - t0
+
+    def run():
+        t0 = time.perf_counter()
+        O.forward(X, A, B, Y0, spec["s"])
+        O.backward_dx_da(X, dY, A, B, spec["s"])
+        O.backward_db(X, A, dY, spec["s"])
+        h = O.shrink(X, a, sl, rk, R, len(osl))
+        O.expand(h, b, sl, rk, sc, y0, osl, R)
+        O.apply_linear(X, a, b, sl, rk, sc, y0, osl, R)
+        O.gather_shrink(gid, ga, gsl, grk, gs["R"])
+        return time.perf_counter() - t0
+
+    return run
 
 
-def cpu_baseline(torch, synth, target_s=12.0):
+def cpu_baseline(torch, synth, tokens=2048, target_s=12.0, max_passes=400):
+    """Oracle throughput on the host cores: passes over a fixed sample of the
+    workload, repeated until about `target_s` seconds of oracle work."""
     from oracle import oracle as O
     O.build()
     cores = O.num_threads()
-    tokens = 64
-    dt = oracle_sample_pass(O, synth, torch, tokens)
-    # grow the sample until one pass takes a few seconds (bounded)
-    while dt < target_s / 4 and tokens < 2048:
-        tokens = min(2048, tokens * 4)
-        dt = oracle_sample_pass(O, synth, torch, tokens)
-    return {"value": tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{tokens} of the 8192 tokens through every op of the step (fp64, one pass, {dt:.2f} s)"}
+    run = oracle_sample(O, synth, torch, tokens)
+    run()   # first touch of the inputs and the library
+    tot, passes = 0.0, 0
+    while tot < target_s and passes < max_passes:
+        tot += run()
+        passes += 1
+    return {"value": tokens * passes / tot, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{tokens} of the 8192 tokens through every op of the step, {passes} passes, "
+                      f"{tot:.1f} s of fp64 oracle work"}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -314,9 +323,10 @@ def run_reference(args, rank, world):
     O.build()
     cores = O.num_threads()
     tokens = 256
+    run = oracle_sample(O, synth, torch, tokens)
     for _ in range(args.warmup):
-        oracle_sample_pass(O, synth, torch, 64)
-    times = [oracle_sample_pass(O, synth, torch, tokens) for _ in range(args.steps)]
+        run()
+    times = [run() for _ in range(args.steps)]
     tot = sum(times)
     value = tokens * len(times) / tot
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
