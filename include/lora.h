@@ -165,6 +165,33 @@ LORA_API lora_status_t lora_backward(lora_dtype_t dtype, int64_t M, int64_t K, i
                           void *ws, size_t ws_bytes, void *stream);
 
 /* --------------------------------------------------------------------------------
+ * lora_backward_ex:  lora_backward with output options, the `dtype` choice of the
+ * [NeMo lora_kernel] update wrappers (lora_da_dx_update_wrapper and
+ * lora_db_update_wrapper take the dtype of the gradients they return) and an
+ * accumulating dX for a layer input that other branches also feed:
+ *   LORA_BWD_DX_ACCUMULATE   dX += scale * dyb*A^T (dX is read, then written;
+ *                            one rounding of the sum to dX's dtype per element);
+ *                            without it dX is overwritten as by lora_backward.
+ *   LORA_BWD_GRAD_INPUT_DTYPE  dA and dB are written in `dtype` (bf16 for
+ *                            LORA_BF16, rounded to nearest even once from the
+ *                            fp32 sums); without it they are float32.
+ *   dA, dB  point to float or to `dtype` elements accordingly (same strides).
+ *   Other arguments, the workspace (LORA_OP_BACKWARD) and errors as lora_backward;
+ *   an unknown bit in flags -> LORA_ERR_INVALID_ARG.
+ * -------------------------------------------------------------------------------- */
+#define LORA_BWD_DX_ACCUMULATE 1u
+#define LORA_BWD_GRAD_INPUT_DTYPE 2u
+LORA_API lora_status_t lora_backward_ex(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r,
+                          const void *X, int64_t ldx, const void *dY, int64_t lddy,
+                          const void *A, int64_t sA_k, int64_t sA_r,
+                          const void *B, int64_t sB_r, int64_t sB_l,
+                          const float *h, int64_t ldh, float scale,
+                          void *dX, int64_t lddx,
+                          void *dA, int64_t sdA_k, int64_t sdA_r,
+                          void *dB, int64_t sdB_r, int64_t sdB_l,
+                          uint32_t flags, void *ws, size_t ws_bytes, void *stream);
+
+/* --------------------------------------------------------------------------------
  * lora_backward_dx_da:  dyb = dY*B^T;  dX = scale * dyb*A^T;  dA = scale * X^T*dyb
  * [NeMo lora_kernel] lora_da_dx_kernel (DYB = DY x B and DX = DY x B x A, with
  * lora_B and lora_A passed transposed) and lora_da_dx_update_wrapper (dlora_A

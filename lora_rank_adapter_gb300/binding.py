@@ -19,12 +19,13 @@ LORA_F32, LORA_BF16 = 0, 1
 OP_FORWARD, OP_BACKWARD_DX_DA, OP_BACKWARD_DB, OP_GROUP_BY_SLOT = 0, 1, 2, 3
 OP_SHRINK, OP_EXPAND, OP_APPLY_LINEAR, OP_GATHER_SHRINK = 4, 5, 6, 7
 OP_BACKWARD = 8
+BWD_DX_ACCUMULATE, BWD_GRAD_INPUT_DTYPE = 1, 2   # lora_backward_ex flags
 STATUS = {0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_UNSUPPORTED", 3: "LORA_ERR_ALIGNMENT",
           4: "LORA_ERR_WORKSPACE", 5: "LORA_ERR_CUDA", 6: "LORA_ERR_DEVICE"}
 EXPORTS = ["lora_workspace_size", "lora_forward", "lora_backward_dx_da", "lora_backward_db",
            "lora_group_by_slot", "lora_shrink", "lora_expand", "lora_apply_linear",
            "lora_gather_shrink", "lora_status_string", "lora_device_error", "lora_kernel_launches",
-           "lora_version", "lora_backward_db_noalloc", "lora_forward_h", "lora_backward"]
+           "lora_version", "lora_backward_db_noalloc", "lora_forward_h", "lora_backward", "lora_backward_ex"]
 
 
 class LoraError(RuntimeError):
@@ -65,6 +66,8 @@ def lib():
                                  P, i64, P, sz, P]),
         "lora_backward": (i32, [i32, i64, i64, i64, i32, P, i64, P, i64, P, i64, i64, P, i64, i64, P, i64,
                                 f32, P, i64, P, i64, i64, P, i64, i64, P, sz, P]),
+        "lora_backward_ex": (i32, [i32, i64, i64, i64, i32, P, i64, P, i64, P, i64, i64, P, i64, i64, P, i64,
+                                   f32, P, i64, P, i64, i64, P, i64, i64, ctypes.c_uint32, P, sz, P]),
         "lora_group_by_slot": (i32, [AP, P, P, P, P, P, sz, P]),
         "lora_shrink": (i32, [AP, P, i64, i32, P, i64, P, i64, i64, P, i64, P, sz, P]),
         "lora_expand": (i32, [AP, P, P, P, i32, P, i64, P, i64, i64, i64, P, i64, P, sz, P]),
@@ -166,6 +169,27 @@ def lora_backward(X, dY, A, B, h, scale, dX, dA, dB, ws=None, stream=None):
                              _ptr(dA), dA.stride(0), dA.stride(1), _ptr(dB), dB.stride(0), dB.stride(1),
                              *_ws_args(ws), _stream(stream))
     _check(st, "lora_backward")
+    return dX, dA, dB
+
+
+def lora_backward_ex(X, dY, A, B, h, scale, dX, dA, dB, flags=0, ws=None, stream=None):
+    """lora_backward with output options: flags BWD_DX_ACCUMULATE (dX += the
+    update) and BWD_GRAD_INPUT_DTYPE (dA, dB in X's dtype instead of fp32)."""
+    M, K = X.shape
+    r, L = B.shape
+    assert dY.shape == (M, L) and A.shape == (K, r) and dX.shape == (M, K) and dA.shape == (K, r)
+    assert dB.shape == (r, L) and h.shape == (M, r) and h.stride(1) == 1 and h.dtype == torch.float32
+    gdt = X.dtype if flags & BWD_GRAD_INPUT_DTYPE else torch.float32
+    assert dA.dtype == gdt and dB.dtype == gdt, (dA.dtype, dB.dtype, gdt)
+    dt = _dtype(X)
+    if ws is None:
+        ws = workspace(OP_BACKWARD, dt, M, K, L, r, device=X.device)
+    st = lib().lora_backward_ex(dt, M, K, L, r, _ptr(X), X.stride(0), _ptr(dY), dY.stride(0),
+                                _ptr(A), A.stride(0), A.stride(1), _ptr(B), B.stride(0), B.stride(1),
+                                _ptr(h), h.stride(0), float(scale), _ptr(dX), dX.stride(0),
+                                _ptr(dA), dA.stride(0), dA.stride(1), _ptr(dB), dB.stride(0), dB.stride(1),
+                                int(flags), *_ws_args(ws), _stream(stream))
+    _check(st, "lora_backward_ex")
     return dX, dA, dB
 
 

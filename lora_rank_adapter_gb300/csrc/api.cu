@@ -231,12 +231,17 @@ lora_status_t lora_forward_h(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L
   return dtype == LORA_BF16 ? forward_bf16(a, ws, ws_bytes, st) : forward_f32(a, st);
 }
 
-lora_status_t lora_backward(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r, const void *X, int64_t ldx,
-                            const void *dY, int64_t lddy, const void *A, int64_t sA_k, int64_t sA_r, const void *B,
-                            int64_t sB_r, int64_t sB_l, const float *h, int64_t ldh, float scale, void *dX,
-                            int64_t lddx, float *dA, int64_t sdA_k, int64_t sdA_r, float *dB, int64_t sdB_r,
-                            int64_t sdB_l, void *ws, size_t ws_bytes, void *stream) {
+lora_status_t lora_backward_ex(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r, const void *X,
+                               int64_t ldx, const void *dY, int64_t lddy, const void *A, int64_t sA_k, int64_t sA_r,
+                               const void *B, int64_t sB_r, int64_t sB_l, const float *h, int64_t ldh, float scale,
+                               void *dX, int64_t lddx, void *dA, int64_t sdA_k, int64_t sdA_r, void *dB,
+                               int64_t sdB_r, int64_t sdB_l, uint32_t flags, void *ws, size_t ws_bytes,
+                               void *stream) {
   LORA_TRY(check_single_common(dtype, M, K, L, r));
+  if (flags & ~(LORA_BWD_DX_ACCUMULATE | LORA_BWD_GRAD_INPUT_DTYPE)) return LORA_ERR_INVALID_ARG;
+  const bool acc = (flags & LORA_BWD_DX_ACCUMULATE) != 0;
+  // gradients in the input dtype: bf16 for LORA_BF16 (float32 inputs keep float32)
+  const lora_dtype_t gdt = (flags & LORA_BWD_GRAD_INPUT_DTYPE) ? dtype : LORA_F32;
   const int e = dtype == LORA_BF16 ? 2 : 4;
   LORA_TRY(check_big(X, M, K, ldx, e));
   LORA_TRY(check_big(dY, M, L, lddy, e));
@@ -246,21 +251,32 @@ lora_status_t lora_backward(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L,
   if (M > 0 && r > 0 && (h == nullptr || ldh < r)) return LORA_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   if (M == 0 || K == 0 || L == 0 || r == 0) {
-    // an empty sum somewhere: the calls that handle it compute what is left
-    LORA_TRY(lora_backward_dx_da(dtype, M, K, L, r, X, ldx, dY, lddy, A, sA_k, sA_r, B, sB_r, sB_l, scale, dX, lddx,
-                                 dA, sdA_k, sdA_r, ws, ws_bytes, stream));
-    // dB is an empty sum (M == 0), empty (L or r == 0), or zero with h = X * A = 0 (K == 0)
-    return fill_zero_2d(LORA_F32, dB, r, L, sdB_r, sdB_l, st);
+    // dyb = 0 or empty: the dX update is zero, and dA and dB are empty or zero sums
+    // (dB's h = X * A is zero when K == 0)
+    if (!acc) LORA_TRY(fill_zero_2d(dtype, dX, M, K, lddx, 1, st));
+    LORA_TRY(fill_zero_2d(gdt, dA, K, r, sdA_k, sdA_r, st));
+    return fill_zero_2d(gdt, dB, r, L, sdB_r, sdB_l, st);
   }
   if (A == nullptr || B == nullptr) return LORA_ERR_INVALID_ARG;
   SingleArgs a{};
   a.dtype = dtype; a.M = M; a.K = K; a.L = L; a.r = r;
   a.X = X; a.ldx = ldx; a.dY = dY; a.lddy = lddy; a.A = A; a.sA_k = sA_k; a.sA_r = sA_r;
   a.B = B; a.sB_r = sB_r; a.sB_l = sB_l; a.scale = scale; a.dX = dX; a.lddx = lddx;
-  a.dA = dA; a.sdA_k = sdA_k; a.sdA_r = sdA_r; a.dB = dB; a.sdB_r = sdB_r; a.sdB_l = sdB_l;
+  a.dA = (float *)dA; a.sdA_k = sdA_k; a.sdA_r = sdA_r; a.dB = (float *)dB; a.sdB_r = sdB_r; a.sdB_l = sdB_l;
   a.h = const_cast<float *>(h); a.ldh = ldh;
+  a.dx_acc = acc ? 1 : 0;
+  a.grad_lo = gdt == LORA_BF16 ? 1 : 0;
   LORA_TRY(check_ws(ws, ws_bytes, single_ws_needed(LORA_OP_BACKWARD, a)));
   return dtype == LORA_BF16 ? backward_bf16(a, ws, ws_bytes, st) : backward_f32(a, ws, ws_bytes, st);
+}
+
+lora_status_t lora_backward(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r, const void *X, int64_t ldx,
+                            const void *dY, int64_t lddy, const void *A, int64_t sA_k, int64_t sA_r, const void *B,
+                            int64_t sB_r, int64_t sB_l, const float *h, int64_t ldh, float scale, void *dX,
+                            int64_t lddx, float *dA, int64_t sdA_k, int64_t sdA_r, float *dB, int64_t sdB_r,
+                            int64_t sdB_l, void *ws, size_t ws_bytes, void *stream) {
+  return lora_backward_ex(dtype, M, K, L, r, X, ldx, dY, lddy, A, sA_k, sA_r, B, sB_r, sB_l, h, ldh, scale, dX, lddx,
+                          dA, sdA_k, sdA_r, dB, sdB_r, sdB_l, 0u, ws, ws_bytes, stream);
 }
 
 lora_status_t lora_backward_dx_da(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r, const void *X,

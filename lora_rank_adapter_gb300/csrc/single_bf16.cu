@@ -574,7 +574,7 @@ struct ColCfg {
   static constexpr int BYTES = 1024 + NS * STAGE + SMALL + RED + 8 * (3 * NS + 1) + 16;
 };
 
-template <int RP>
+template <int RP, bool kAccX>   // kAccX: dX += the update (p.dx_old), else dX = the update
 __global__ void __launch_bounds__(NTHREADS_LS) colpass_dxda_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                    const __grid_constant__ CUtensorMap tmA,
                                                                    const __grid_constant__ CUtensorMap tmDX,
@@ -710,9 +710,21 @@ __global__ void __launch_bounds__(NTHREADS_LS) colpass_dxda_kernel(const __grid_
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          uint32_t *dp = reinterpret_cast<uint32_t *>(
-              st + tile_off(mh * 32 + mt * 16 + gq + 8 * hf, kh * 32 + nt * 8 + 2 * cq));
-          *dp = pack_bf16(scale * acc[mt][nt][2 * hf], scale * acc[mt][nt][2 * hf + 1]);
+          const int tr = mh * 32 + mt * 16 + gq + 8 * hf, tc = kh * 32 + nt * 8 + 2 * cq;
+          uint32_t *dp = reinterpret_cast<uint32_t *>(st + tile_off(tr, tc));
+          float v0 = scale * acc[mt][nt][2 * hf], v1 = scale * acc[mt][nt][2 * hf + 1];
+          if (kAccX) {
+            // accumulate: the pair (row, col), (row, col + 1) of dX before this call
+            // (col is even and rows of dX are 16-byte aligned, so the pair is in the row)
+            const int64_t row = (int64_t)(t_beg + g) * BM + tr;
+            const int col = k0 + tc;
+            if (row < p.M && col < p.K) {
+              const float2 o = unpack_bf16(*reinterpret_cast<const unsigned int *>(p.dx_old + row * p.lddx + col));
+              v0 += o.x;
+              v1 += o.y;
+            }
+          }
+          *dp = pack_bf16(v0, v1);
         }
     fence_proxy_async_smem();
     __syncwarp();
@@ -759,7 +771,9 @@ __global__ void __launch_bounds__(NTHREADS_LS) colpass_dxda_kernel(const __grid_
       if (k >= p.K || j >= p.r) continue;
       float v = 0.f;
       for (int q = 0; q < p.msplit; ++q) v += __ldcg(&p.part_out[((int64_t)q * kpad + k) * RP + j]);
-      p.out[(int64_t)k * p.out_s0 + (int64_t)j * p.out_s1] = scale * v;
+      const int64_t o = (int64_t)k * p.out_s0 + (int64_t)j * p.out_s1;
+      if (p.out_bf16) reinterpret_cast<__nv_bfloat16 *>(p.out)[o] = __float2bfloat16_rn(scale * v);
+      else p.out[o] = scale * v;
     }
     if (threadIdx.x == 0) p.counters[kb] = 0;
   }
@@ -880,7 +894,9 @@ __global__ void __launch_bounds__(NTHREADS) colpass_db_kernel(const __grid_const
       if (j >= p.r || l >= p.K) continue;   // p.K holds L for this kernel
       float v = 0.f;
       for (int q = 0; q < p.msplit; ++q) v += __ldcg(&p.part_out[((int64_t)q * RP + j) * lpad + l]);
-      p.out[(int64_t)j * p.out_s0 + (int64_t)l * p.out_s1] = scale * v;
+      const int64_t o = (int64_t)j * p.out_s0 + (int64_t)l * p.out_s1;
+      if (p.out_bf16) reinterpret_cast<__nv_bfloat16 *>(p.out)[o] = __float2bfloat16_rn(scale * v);
+      else p.out[o] = scale * v;
     }
     if (threadIdx.x == 0) p.counters[lb] = 0;
   }
@@ -1086,7 +1102,7 @@ static lora_status_t dxda_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cud
   if (!blob || !partA || !counters) return LORA_ERR_WORKSPACE;
   LORA_TRY((launch_rows<RP, true>(a.dY, a.lddy, a.L, tB, a.M, blob, counters, (int)nkb, st)));
 
-  auto kern = colpass_dxda_kernel<RP>;
+  auto kern = a.dx_acc ? colpass_dxda_kernel<RP, true> : colpass_dxda_kernel<RP, false>;
   const size_t smem = ColCfg<RP>::BYTES;
   LORA_CUDA(ensure_smem((const void *)kern, smem));
   const int ms = choose_msplit(nkb, a.M, (const void *)kern, NTHREADS_LS, smem);
@@ -1104,7 +1120,10 @@ static lora_status_t dxda_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cud
   p.out = a.dA;
   p.out_s0 = a.sdA_k;
   p.out_s1 = a.sdA_r;
+  p.out_bf16 = a.grad_lo;
   p.blob = blob;
+  p.dx_old = a.dx_acc ? (const __nv_bfloat16 *)a.dX : nullptr;
+  p.lddx = a.lddx;
   LORA_CUDA(launch(kern, dim3((unsigned)(nkb * ms)), dim3(NTHREADS_LS), smem, st, 1, true, tX, tA, tDX, p));
   return LORA_OK;
 }
@@ -1160,6 +1179,7 @@ static lora_status_t launch_colpass_db(const SingleArgs &a, const uint8_t *blob,
   p.part_out = partB;
   p.counters = counters;
   p.out = a.dB;
+  p.out_bf16 = a.grad_lo;
   p.out_s0 = a.sdB_r;
   p.out_s1 = a.sdB_l;
   p.blob = const_cast<uint8_t *>(blob);

@@ -2,6 +2,7 @@
 // kernels and the C ABI layer.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -25,6 +26,8 @@ struct SingleArgs {
   float *dB; int64_t sdB_r, sdB_l;
   float scale;
   float *h; int64_t ldh;      // forward: optional h = X * A out; backward: the saved h in
+  int dx_acc = 0;             // backward: dX += the update (else dX = the update)
+  int grad_lo = 0;            // backward: dA and dB in the input dtype (bf16), else fp32
 };
 
 // Whether A / B are repacked into the workspace, and the row strides used.
@@ -54,9 +57,12 @@ struct ColArgs {
   float scale;
   float *part_out;
   int *counters;
-  float *out;
+  float *out;                 // bf16 elements when out_bf16
   int64_t out_s0, out_s1;
+  int out_bf16;
   const uint8_t *blob;        // the row pass's hi/lo tiles of dyb (dX/dA) or h (dB)
+  const __nv_bfloat16 *dx_old;   // dX pass: dX to add to (nullptr: overwrite)
+  int64_t lddx;
 };
 
 SingleLayout plan_layout(const SingleArgs &a, bool need_A, bool need_B);

@@ -82,7 +82,8 @@ __global__ void __launch_bounds__(256) dx_f32_kernel(SingleArgs a, const float *
     const int64_t m = e / a.K, k = e % a.K;
     float acc = 0.f;
     for (int j = 0; j < a.r; ++j) acc += dyb[m * a.r + j] * A[k * a.sA_k + j * a.sA_r];
-    dX[m * a.lddx + k] = a.scale * acc;
+    const float v = a.scale * acc;
+    dX[m * a.lddx + k] = a.dx_acc ? dX[m * a.lddx + k] + v : v;
   }
   pdl_launch_dependents();
 }

@@ -109,6 +109,18 @@ def backward_db(X, A, dY, s, lib=None):
     return dB
 
 
+def backward_ex(X, dY, A, B, s, dX0=None, lib=None):
+    """The backward with its output options ([NeMo lora_kernel] update wrappers,
+    whose `dtype` picks the gradients' type; an accumulating dX): returns
+    (dX0 + s*dY B^T A^T, or that update alone when dX0 is None), dA and dB in
+    fp64.  The gradients' storage type is the caller's rounding, not the oracle's."""
+    dX, dA = backward_dx_da(X, dY, A, B, s, lib)
+    dB = backward_db(X, A, dY, s, lib)
+    if dX0 is not None:
+        dX = _f64(dX0) + dX
+    return dX, dA, dB
+
+
 def group_by_slot(slots, ranks, R, lib=None):
     slots, ranks = _i32(slots), _i32(ranks)
     T, S = slots.shape[0], ranks.shape[0]

@@ -17,7 +17,7 @@ def L():
 
 def test_every_declared_symbol_is_exported(L):
     declared = header_functions()
-    assert len(declared) == 16, declared
+    assert len(declared) == 17, declared
     assert sorted(B.EXPORTS) == declared
     for name in declared:
         assert hasattr(L, name), name
@@ -97,6 +97,13 @@ def test_fused_argument_errors(L):
     assert bw() == 4                               # needs workspace
     need = L.lora_workspace_size(B.OP_BACKWARD, 1, 64, 64, 64, 16, 0)
     assert need >= L.lora_workspace_size(B.OP_BACKWARD_DX_DA, 1, 64, 64, 64, 16, 0)
+    bx = lambda **k: L.lora_backward_ex(k.get("dt", 1), k.get("M", 64), 64, 64, 16, FAKE, 64, FAKE, 64, FAKE, 1, 64,
+                                        FAKE, 1, 16, FAKE, 16, 1.0, FAKE, 64, k.get("dA", FAKE), 16, 1, FAKE, 64,
+                                        1, k.get("flags", 0), k.get("ws", NULL), k.get("wsb", 0), S0)
+    assert bx(flags=4) == 1                        # unknown flag
+    assert bx(flags=3, dA=NULL) == 1               # dA still required
+    assert bx(flags=3) == 4                        # needs the lora_backward workspace
+    assert bx(flags=1) == 4
 
 
 def test_workspace_sizes_monotone(L):

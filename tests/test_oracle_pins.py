@@ -105,6 +105,23 @@ def test_backward_dense_association(M, K, L, r):
     assert _rel(O.backward_db(X, A, dY, s), s * A.T @ dW) < 1e-12
 
 
+@pytest.mark.parametrize("M,K,L,r", SHAPES)
+def test_backward_ex_accumulates_dense_gradient(M, K, L, r):
+    # the accumulating dX is dX0 plus dY W^T of the dense weight; dA, dB as the backward
+    rng = np.random.default_rng(300 + M * 31 + K * 7 + L * 3 + r)
+    X, A, B, _, dY = _rand_single(rng, M, K, L, r)
+    dX0 = rng.standard_normal((M, K))
+    s = 0.5
+    W = s * (A @ B)
+    dW = X.T @ dY
+    dX, dA, dB = O.backward_ex(X, dY, A, B, s, dX0)
+    assert _rel(dX, dX0 + dY @ W.T) < 1e-12
+    assert _rel(dA, s * dW @ B.T) < 1e-12
+    assert _rel(dB, s * A.T @ dW) < 1e-12
+    dXo, _, _ = O.backward_ex(X, dY, A, B, s)
+    assert _rel(dXo, dY @ W.T) < 1e-12
+
+
 def test_rank1_closed_form():
     rng = np.random.default_rng(7)
     M, K, L = 4, 5, 6

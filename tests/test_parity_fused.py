@@ -150,3 +150,82 @@ def test_fused_degenerate_shapes():
                        torch.empty((0, 24), dtype=torch.bfloat16, device=DEV), dA, dB2)
     torch.cuda.synchronize()
     assert torch.all(hz == 0) and torch.all(dB == 0) and torch.all(dA == 0) and torch.all(dB2 == 0)
+
+
+# ----------------------------------------------------------------------------- output options
+def _grad_bufs(K, r, L, dt):
+    dAbuf = torch.full((K + 2, r + 3), SENT, dtype=dt, device=DEV)
+    dBbuf = torch.full((r + 2, L + 3), SENT, dtype=dt, device=DEV)
+    return dAbuf, dBbuf, dAbuf[:K, :r], dBbuf[:r, :L]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("flags", [1, 2, 3])
+@pytest.mark.parametrize("M,K,L,r", [(3, 24, 40, 3), (130, 200, 72, 16), (300, 136, 200, 64), (129, 256, 192, 128)])
+def test_backward_ex_options(M, K, L, r, flags, dtype):
+    """lora_backward_ex: dX accumulated onto a prior dX of the update's own size
+    (so the check sees the update), and dA / dB in the input dtype."""
+    w = workload(M, K, L, r, dtype, 11 + M + r)
+    s = 2.0
+    X, A, B, dY = w["X"], w["A"], w["B"], w["dY"]
+    h = torch.empty((M, r), dtype=torch.float32, device=DEV)
+    lora.lora_forward_h(X, A, B, w["Y0"].clone(), s, h)
+    acc = bool(flags & lora.BWD_DX_ACCUMULATE)
+    upd, _ = O.backward_dx_da(f64(X), f64(dY), f64(A), f64(B), s)
+    sigma = float(np.max(np.abs(upd))) / 2 or 1.0
+    dX0 = synth.draw(("normal", sigma), (M, K), 7, "g.dX0", dtype, DEV)
+    dXv, dXbuf = padded(dX0, 3, 5)
+    gdt = X.dtype if flags & lora.BWD_GRAD_INPUT_DTYPE else torch.float32
+    dAbuf, dBbuf, dA, dB = _grad_bufs(K, r, L, gdt)
+    lora.lora_backward_ex(X, dY, A, B, h, s, dXv, dA, dB, flags=flags)
+    torch.cuda.synchronize()
+    assert lora.lora_device_error() == 0
+    rdX, rdA, rdB = O.backward_ex(f64(X), f64(dY), f64(A), f64(B), s, f64(dX0) if acc else None)
+    lo = dtype == "bf16"
+    tol_g = TOL_BF16 if (lo and gdt != torch.float32) else TOL_F32
+    assert rel_err(f64(dXv), rdX) <= (TOL_BF16 if lo else TOL_F32)
+    assert rel_err(f64(dA), rdA) <= tol_g and rel_err(f64(dB), rdB) <= tol_g
+    assert untouched(dXbuf, M, K) and untouched(dAbuf, K, r) and untouched(dBbuf, r, L)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_backward_ex_rounding_relations(dtype):
+    """The bf16 gradients are the fp32 gradients rounded once (bit-exact), and an
+    accumulation onto zeros is the overwriting backward (bit-exact)."""
+    w = workload(257, 264, 392, 24, dtype, 3)
+    X, A, B, dY = w["X"], w["A"], w["B"], w["dY"]
+    M, K = X.shape
+    r, L = B.shape
+    h = torch.empty((M, r), dtype=torch.float32, device=DEV)
+    lora.lora_forward_h(X, A, B, w["Y0"].clone(), 0.5, h)
+    dX1, dA1, dB1 = torch.empty_like(X), torch.empty((K, r), device=DEV), torch.empty((r, L), device=DEV)
+    lora.lora_backward(X, dY, A, B, h, 0.5, dX1, dA1, dB1)
+    dX2 = torch.zeros_like(X)
+    dA2 = torch.empty((K, r), dtype=X.dtype, device=DEV)
+    dB2 = torch.empty((r, L), dtype=X.dtype, device=DEV)
+    lora.lora_backward_ex(X, dY, A, B, h, 0.5, dX2, dA2, dB2, flags=3)
+    torch.cuda.synchronize()
+    assert torch.equal(dX1, dX2)
+    assert torch.equal(dA1.to(X.dtype), dA2) and torch.equal(dB1.to(X.dtype), dB2)
+
+
+def test_backward_ex_degenerate_shapes():
+    """L = 0: the dX update is zero (an accumulated dX keeps its values), dA = 0 and
+    dB is empty; M = 0: dA = 0 and dB = 0, in bf16."""
+    X = synth.draw(("normal", 1.0), (40, 24), 0, "g.X", "bf16", DEV)
+    A = synth.draw(("normal", 1.0), (24, 4), 0, "g.A", "bf16", DEV)
+    dX0 = synth.draw(("normal", 1.0), (40, 24), 1, "g.dX0", "bf16", DEV)
+    dX = dX0.clone()
+    dA = torch.full((24, 4), 3.0, dtype=torch.bfloat16, device=DEV)
+    h = torch.zeros((40, 4), device=DEV)
+    lora.lora_backward_ex(X, torch.empty((40, 0), dtype=torch.bfloat16, device=DEV), A,
+                          torch.empty((4, 0), dtype=torch.bfloat16, device=DEV), h, 1.0, dX, dA,
+                          torch.empty((4, 0), dtype=torch.bfloat16, device=DEV), flags=3)
+    dA2 = torch.full((24, 4), 3.0, dtype=torch.bfloat16, device=DEV)
+    dB2 = torch.full((4, 16), 3.0, dtype=torch.bfloat16, device=DEV)
+    B = synth.draw(("normal", 1.0), (4, 16), 0, "g.B", "bf16", DEV)
+    lora.lora_backward_ex(X[:0], torch.empty((0, 16), dtype=torch.bfloat16, device=DEV), A, B,
+                          torch.empty((0, 4), device=DEV), 1.0, torch.empty((0, 24), dtype=torch.bfloat16, device=DEV),
+                          dA2, dB2, flags=3)
+    torch.cuda.synchronize()
+    assert torch.equal(dX, dX0) and torch.all(dA == 0) and torch.all(dA2 == 0) and torch.all(dB2 == 0)
