@@ -7,9 +7,13 @@
  * CUDA library; both sides only see the same seeded input arrays.
  *
  * Every function works in double precision on dense row-major arrays that hold
- * the exact (widened) values of the inputs.  Loops are plain and ascending; the
- * only parallelism is OpenMP over independent output rows, so each output
- * element is summed in one fixed order.
+ * the exact (widened) values of the inputs.  Every output element is one sum
+ * over its contraction index in ascending order, started from 0.0 and scaled
+ * once at the end; the loops are nested so that inner loops walk contiguous
+ * memory, and the only parallelism is OpenMP over independent output rows or
+ * blocks of output elements, so the order of each sum is fixed.  The build
+ * turns off floating-point contraction (no fused multiply-add), so results
+ * are the same on every host.
  *
  * Sources (cited by page title and API entry):
  *   [NeMo lora_kernel] "nemo_automodel.components._peft.lora_kernel" API page:
@@ -41,6 +45,11 @@
 #ifdef _OPENMP
 #include <omp.h>
 #endif
+
+/* Rows of dA / columns of dB whose running sums one thread keeps together
+ * (cache blocking only: every element is still one ascending sum). */
+#define ORACLE_KB 64
+#define ORACLE_LB 256
 
 int oracle_num_threads(void)
 {
@@ -79,19 +88,28 @@ void oracle_lora_forward(int64_t M, int64_t K, int64_t L, int64_t r,
                          const double *X, const double *A, const double *B,
                          const double *Y0, double s, double *Y)
 {
-    #pragma omp parallel for schedule(static)
-    for (int64_t m = 0; m < M; ++m) {
+    /* Every sum runs over its contraction index in ascending order, starting
+     * from 0.0; the loops are nested so that the inner loop walks contiguous
+     * memory (h[j] and acc[l] are the running sums of their elements). */
+    #pragma omp parallel
+    {
         double *h = (double *)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
-        for (int64_t j = 0; j < r; ++j) {
-            double acc = 0.0;
-            for (int64_t k = 0; k < K; ++k) acc += X[m * K + k] * A[k * r + j];
-            h[j] = acc;
+        double *acc = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        #pragma omp for schedule(static)
+        for (int64_t m = 0; m < M; ++m) {
+            for (int64_t j = 0; j < r; ++j) h[j] = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double xk = X[m * K + k];
+                for (int64_t j = 0; j < r; ++j) h[j] += xk * A[k * r + j];
+            }
+            for (int64_t l = 0; l < L; ++l) acc[l] = 0.0;
+            for (int64_t j = 0; j < r; ++j) {
+                const double hj = h[j];
+                for (int64_t l = 0; l < L; ++l) acc[l] += hj * B[j * L + l];
+            }
+            for (int64_t l = 0; l < L; ++l) Y[m * L + l] = Y0[m * L + l] + s * acc[l];
         }
-        for (int64_t l = 0; l < L; ++l) {
-            double acc = 0.0;
-            for (int64_t j = 0; j < r; ++j) acc += h[j] * B[j * L + l];
-            Y[m * L + l] = Y0[m * L + l] + s * acc;
-        }
+        free(acc);
         free(h);
     }
 }
@@ -124,13 +142,21 @@ void oracle_lora_backward_dx_da(int64_t M, int64_t K, int64_t L, int64_t r,
             dX[m * K + k] = s * acc;
         }
     }
+    /* dA[k][j] = s * (sum over m ascending of X[m][k] * dyb[m][j]); the rows k
+     * are taken in blocks of ORACLE_KB so that a block's running sums stay in
+     * cache while m advances. */
     #pragma omp parallel for schedule(static)
-    for (int64_t k = 0; k < K; ++k) {
-        for (int64_t j = 0; j < r; ++j) {
-            double acc = 0.0;
-            for (int64_t m = 0; m < M; ++m) acc += X[m * K + k] * dyb[m * r + j];
-            dA[k * r + j] = s * acc;
-        }
+    for (int64_t k0 = 0; k0 < K; k0 += ORACLE_KB) {
+        const int64_t k1 = k0 + ORACLE_KB < K ? k0 + ORACLE_KB : K;
+        for (int64_t k = k0; k < k1; ++k)
+            for (int64_t j = 0; j < r; ++j) dA[k * r + j] = 0.0;
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t k = k0; k < k1; ++k) {
+                const double xk = X[m * K + k];
+                for (int64_t j = 0; j < r; ++j) dA[k * r + j] += xk * dyb[m * r + j];
+            }
+        for (int64_t k = k0; k < k1; ++k)
+            for (int64_t j = 0; j < r; ++j) dA[k * r + j] = s * dA[k * r + j];
     }
     free(dyb);
 }
@@ -145,21 +171,30 @@ void oracle_lora_backward_db(int64_t M, int64_t K, int64_t L, int64_t r,
                              double s, double *dB)
 {
     double *h = (double *)malloc(sizeof(double) * (size_t)(M * r > 0 ? M * r : 1));
+    /* h[m][j] = sum over k ascending of X[m][k] * A[k][j] */
     #pragma omp parallel for schedule(static)
     for (int64_t m = 0; m < M; ++m) {
-        for (int64_t j = 0; j < r; ++j) {
-            double acc = 0.0;
-            for (int64_t k = 0; k < K; ++k) acc += X[m * K + k] * A[k * r + j];
-            h[m * r + j] = acc;
+        double *hm = h + m * r;
+        for (int64_t j = 0; j < r; ++j) hm[j] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double xk = X[m * K + k];
+            for (int64_t j = 0; j < r; ++j) hm[j] += xk * A[k * r + j];
         }
     }
+    /* dB[j][l] = s * (sum over m ascending of h[m][j] * dY[m][l]), the columns l
+     * in blocks of ORACLE_LB whose running sums stay in cache while m advances */
     #pragma omp parallel for schedule(static)
-    for (int64_t j = 0; j < r; ++j) {
-        for (int64_t l = 0; l < L; ++l) {
-            double acc = 0.0;
-            for (int64_t m = 0; m < M; ++m) acc += h[m * r + j] * dY[m * L + l];
-            dB[j * L + l] = s * acc;
-        }
+    for (int64_t l0 = 0; l0 < L; l0 += ORACLE_LB) {
+        const int64_t l1 = l0 + ORACLE_LB < L ? l0 + ORACLE_LB : L;
+        for (int64_t j = 0; j < r; ++j)
+            for (int64_t l = l0; l < l1; ++l) dB[j * L + l] = 0.0;
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t j = 0; j < r; ++j) {
+                const double hj = h[m * r + j];
+                for (int64_t l = l0; l < l1; ++l) dB[j * L + l] += hj * dY[m * L + l];
+            }
+        for (int64_t j = 0; j < r; ++j)
+            for (int64_t l = l0; l < l1; ++l) dB[j * L + l] = s * dB[j * L + l];
     }
     free(h);
 }

@@ -26,7 +26,7 @@ def build(force=False, src=_SRC, out=_LIB_PATH):
     os.makedirs(os.path.dirname(out), exist_ok=True)
     if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
         return out
-    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", out, src, "-lm"]
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-o", out, src, "-lm"]
     subprocess.run(cmd, check=True)
     return out
 

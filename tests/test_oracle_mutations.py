@@ -16,14 +16,13 @@ SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), 
                    "lora_oracle.c")
 
 MUTATIONS = [
-    ("fwd_transposed_A", "acc += X[m * K + k] * A[k * r + j];\n            h[j] = acc;",
-     "acc += X[m * K + k] * A[j * K + k];\n            h[j] = acc;"),
-    ("fwd_sign", "Y[m * L + l] = Y0[m * L + l] + s * acc;", "Y[m * L + l] = Y0[m * L + l] - s * acc;"),
-    ("fwd_index_B", "acc += h[j] * B[j * L + l];", "acc += h[j] * B[j * L + 0];"),
+    ("fwd_transposed_A", ") h[j] += xk * A[k * r + j];", ") h[j] += xk * A[j * K + k];"),
+    ("fwd_sign", "Y[m * L + l] = Y0[m * L + l] + s * acc[l];", "Y[m * L + l] = Y0[m * L + l] - s * acc[l];"),
+    ("fwd_index_B", "acc[l] += hj * B[j * L + l];", "acc[l] += hj * B[j * L + 0];"),
     ("dx_dropped_scale", "dX[m * K + k] = s * acc;", "dX[m * K + k] = acc;"),
     ("dx_transposed_B", "acc += dY[m * L + l] * B[j * L + l];", "acc += dY[m * L + l] * B[l * r + j];"),
-    ("da_index", "acc += X[m * K + k] * dyb[m * r + j];", "acc += X[m * K + k] * dyb[m * r + 0];"),
-    ("db_index", "acc += h[m * r + j] * dY[m * L + l];", "acc += h[m * r + j] * dY[m * L + 0];"),
+    ("da_index", "dA[k * r + j] += xk * dyb[m * r + j];", "dA[k * r + j] += xk * dyb[m * r + 0];"),
+    ("db_index", "dB[j * L + l] += hj * dY[m * L + l];", "dB[j * L + l] += hj * dY[m * L + 0];"),
     ("shrink_past_rank", "for (int32_t j = 0; j < rank; ++j) {\n                const double *arow",
      "for (int32_t j = 0; j < R; ++j) {\n                const double *arow"),
     ("expand_slice_offset", "bs[(off + c) * R + j]", "bs[(c) * R + j]"),

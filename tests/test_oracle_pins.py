@@ -139,6 +139,35 @@ def test_rank1_closed_form():
             assert abs(Y[m, l] - (Y0[m, l] + s * xa * bv[l])) <= 1e-12 * (1 + abs(Y[m, l]))
 
 
+def test_single_adapter_sums_run_in_ascending_order():
+    """Each element of the oracle's single-adapter outputs is one sum over its
+    contraction index in ascending order (no reassociation, no fused
+    multiply-add): bit-for-bit what plain Python float loops give.  This guards
+    the loop nesting of the oracle, which is arranged for cache locality; it is
+    a regression check of the summation order, not a pin of the definition."""
+    rng = np.random.default_rng(11)
+    M, K, L, r, s = 5, 7, 6, 3, 0.75
+    X, A, B = rng.standard_normal((M, K)), rng.standard_normal((K, r)), rng.standard_normal((r, L))
+    Y0, dY = rng.standard_normal((M, L)), rng.standard_normal((M, L))
+
+    def dot(n, f):
+        acc = 0.0
+        for i in range(n):
+            acc += f(i)
+        return acc
+
+    h = [[dot(K, lambda k: X[m, k] * A[k, j]) for j in range(r)] for m in range(M)]
+    Y = [[Y0[m, l] + s * dot(r, lambda j: h[m][j] * B[j, l]) for l in range(L)] for m in range(M)]
+    dyb = [[dot(L, lambda l: dY[m, l] * B[j, l]) for j in range(r)] for m in range(M)]
+    dX = [[s * dot(r, lambda j: dyb[m][j] * A[k, j]) for k in range(K)] for m in range(M)]
+    dA = [[s * dot(M, lambda m: X[m, k] * dyb[m][j]) for j in range(r)] for k in range(K)]
+    dB = [[s * dot(M, lambda m: h[m][j] * dY[m, l]) for l in range(L)] for j in range(r)]
+    gdX, gdA = O.backward_dx_da(X, dY, A, B, s)
+    assert np.array_equal(O.forward(X, A, B, Y0, s), np.array(Y))
+    assert np.array_equal(gdX, np.array(dX)) and np.array_equal(gdA, np.array(dA))
+    assert np.array_equal(O.backward_db(X, A, dY, s), np.array(dB))
+
+
 def test_finite_differences_exact():
     """L(X, A, B) = sum(dY * forward(X, A, B, 0)) is linear in each of X, A, B,
     so a central difference is exact up to fp64 rounding for any step."""
