@@ -1,30 +1,36 @@
 #!/usr/bin/env python
-"""Throughput of the LoRA adapter-product hot path on GB300 (one JSON line).
+"""Throughput of the LoRA adapter-product hot path on one GB300 (one JSON line).
 
-Workload: one batch of 8192 tokens x 4096 features in bf16 (the q_proj
-configuration: batch 4 x seq 2048, r = 16, scale 2) pushed through every step
-of the hot path, each through the C ABI of liblora.so:
-  training   lora_forward_h (the forward, saving h = X A) and lora_backward
-             (dX, dA, dB in one call from the saved h), r = 16
-  serving    lora_shrink, lora_expand, lora_apply_linear on the same batch as a
-             fused QKV target (out_slices [4096, 1024, 1024], 32 adapter slots,
-             R = 64, ranks from {0, 8, 16, 32, 64}, contiguous segments of
-             geometric length with mean 128, 10% on the zero adapter), and
-             lora_gather_shrink of the batch's token ids over a 128256-entry
-             embedding axis (5% of ids = -1).
-A step is one pass of all of them; value = tokens per step / step time.
-Inputs are resident in HBM before the timed region; three independent input
-sets (> 3 x 129 MB L2) rotate between steps and the ops of a step use
-different sets, so no op re-reads what the previous op left in L2.
+Headline workload (the timed step): the wide-MLP LoRA training step, bf16,
+16384 tokens, r = 64, scale 0.5, through the C ABI of liblora.so:
+  up_proj   K = 4096 -> L = 14336:  lora_forward_h, then lora_backward
+  down_proj K = 14336 -> L = 4096:  lora_forward_h, then lora_backward
+(the forward adds s (X A) B into Y and saves h = X A; the backward writes dX,
+dA and dB from dY and the saved h).  value = 16384 tokens / step time.
+
+Per-configuration parts (each op timed alone with CUDA events, L2 flushed
+before every launch, median of the repetitions) cover the other seeded
+configurations of the benchmark:
+  c1  fp32 256 x 512 x 512, r = 8:          lora_forward, lora_backward_dx_da, lora_backward_db
+  c2  bf16 q_proj 8192 x 4096 x 4096, r=16: the same three, and lora_forward_h + lora_backward
+  c3  the headline ops, one by one
+  c4  prefill T = 4096, in = 4096, QKV [4096, 1024, 1024], 32 slots (R = 64):
+      lora_group_by_slot, lora_shrink, lora_expand, lora_apply_linear
+  c5  decode T = 256 over 128 slots, in = out = 8192 (R = 64): lora_shrink,
+      lora_expand, lora_apply_linear, and lora_gather_shrink over a
+      128256-entry axis with 5% of the ids = -1
+Each part carries its algorithmic bytes (what must cross HBM once), GB/s and
+the fraction of the measured copy bandwidth.
+
+Inputs are resident in HBM before the timed region; the headline step rotates
+two input sets (every op's operands are larger than the 129 MB L2, and
+consecutive ops read different sets).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 """
 import argparse
 import hashlib
 import json
-import math
-
-import numpy as np
 import os
 import statistics
 import subprocess
@@ -32,28 +38,33 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "LoRA fwd+bwd & multi-adapter shrink/expand tokens/s; % of HBM roofline"
 UNIT = "tokens/s"
-NSETS = 3
 SEED = 0
-WORKLOAD = ("q_proj batch M=8192 x K=4096 bf16 through the whole hot path: fwd+dX/dA+dB (r=16, L=4096), "
-            "group/shrink/expand/apply_linear as fused QKV [4096,1024,1024] over 32 slots (R=64), "
-            "gather_shrink over V=128256")
+NSETS = 2
+WORKLOAD = ("wide-MLP LoRA training step (c3): M=16384 tokens, r=64, s=0.5, bf16; up_proj 4096->14336 and "
+            "down_proj 14336->4096, each lora_forward_h + lora_backward (dX, dA, dB)")
+C3_TOKENS = 16384
 FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--part-reps", type=int, default=30, help="repetitions of each per-configuration part")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="", help="comma-separated op names to run (profiling); default: all")
+    ap.add_argument("--no-parts", action="store_true", help="skip the per-configuration parts")
+    ap.add_argument("--parts", default="", help="comma-separated configurations for the parts (c1..c5)")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA-graph replays")
     return ap.parse_args()
 
@@ -129,50 +140,24 @@ class ClockSampler:
                 "power_w_max": max((num(p[2]) or 0.0) for p in inside)}
 
 
-# ----------------------------------------------------------------------------- workload
-def build_single(torch, synth, dev, k):
-    spec = synth.single_spec("single_c2")
-    w = synth.make_single(spec, seed=SEED + k, device=dev, prefix=f"bench{k}")
-    M, K = w["X"].shape
-    r, L = w["B"].shape
-    # adapter weights in the PEFT layout: lora_A.weight [r, K], lora_B.weight [L, r]
-    w["A"] = w["A"].t().contiguous().t()
-    w["B"] = w["B"].t().contiguous().t()
-    w["Y"] = w["Y0"].clone()
-    w["dX"] = torch.empty_like(w["X"])
-    w["dA"] = torch.empty((K, r), dtype=torch.float32, device=dev)
-    w["dB"] = torch.empty((r, L), dtype=torch.float32, device=dev)
-    w["h"] = torch.empty((M, r), dtype=torch.float32, device=dev)
-    w["s"] = spec["s"]
-    return w
-
-
-def single_bytes(M, K, L, r):
-    """What must cross HBM once: the forward reads X, A, B and reads and writes Y,
-    writing h; the backward reads X, dY, A, B and h and writes dX, dA, dB."""
-    e = 2
+# ----------------------------------------------------------------------------- algorithmic bytes
+def single_bytes(M, K, L, r, e):
+    """What each single-adapter op must move across HBM once (e = element size
+    of X, Y, dY, dX; h, dA and dB are fp32)."""
+    X, Y, Ab, Bb = M * K * e, M * L * e, K * r * e, r * L * e
+    h, dA, dB = M * r * 4, K * r * 4, r * L * 4
     return {
-        "lora_forward_h": M * K * e + 2 * M * L * e + K * r * e + r * L * e + M * r * 4,
-        "lora_backward": M * L * e + 2 * M * K * e + K * r * e + r * L * e + M * r * 4 + K * r * 4 + r * L * 4,
+        "lora_forward": X + 2 * Y + Ab + Bb,
+        "lora_forward_h": X + 2 * Y + Ab + Bb + h,
+        "lora_backward_dx_da": Y + 2 * X + Ab + Bb + dA,      # dY, X, dX
+        "lora_backward_db": X + Y + Ab + dB,                   # X, dY
+        "lora_backward": Y + 2 * X + Ab + Bb + h + dA + dB,    # dY, X, dX (h saved)
     }
 
 
-MULTI_SPEC = dict(T=8192, IN=4096)   # the q_proj batch as a fused-QKV serving target
-
-
-def build_multi(torch, synth, dev, k, X):
-    spec = synth.multi_spec("multi_c4", **MULTI_SPEC)
-    w = synth.make_multi(spec, seed=SEED + k, device=dev)
-    w["x"] = X                                    # the same batch of tokens
-    w["y"] = w["y0"].clone()
-    w["h"] = torch.zeros((spec["T"], len(spec["out_slices"]) * spec["R"]), dtype=torch.float32, device=dev)
-    w["spec"] = spec
-    return w
-
-
 def multi_bytes(w):
-    """Algorithmic bytes: active tokens only, rank-limited columns, each used
-    slot's adapter weights once."""
+    """Algorithmic bytes of the segmented ops: active tokens only, rank-limited
+    columns, each used slot's adapter rows once."""
     slots = w["slots"].cpu().tolist()
     ranks = w["ranks"].cpu().tolist()
     S, R, IN = w["S"], w["R"], w["IN"]
@@ -184,133 +169,171 @@ def multi_bytes(w):
     hcols = sum(n * ranks[slots[t]] for t in act)          # specified h entries
     a_b = sum(n * ranks[s] * IN * 2 for s in used)
     b_b = sum(ranks[s] * O * 2 for s in used)
-    return {
+    out = {
+        "lora_group_by_slot": len(slots) * 4 + S * 4 + na * 4,
         "lora_shrink": na * IN * 2 + a_b + hcols * 4,
         "lora_expand": hcols * 4 + 2 * na * O * 2 + b_b,
         "lora_apply_linear": na * IN * 2 + a_b + b_b + 2 * na * O * 2,
     }
+    if "ga" in w:
+        V = w["V"]
+        ids = w["ids"].cpu().tolist()
+        out["lora_gather_shrink"] = (sum(ranks[s] * (2 + 4) for t, s in enumerate(slots)
+                                         if 0 <= s < S and 1 <= ranks[s] <= R and 0 <= ids[t] < V)
+                                     + 12 * len(slots))
+    return out
 
 
-def make_ops(torch, lora, binding, synth, dev):
-    """Per input set: the list of (name, callable, bytes) that makes one step."""
-    sets = []
-    for k in range(NSETS):
-        w = build_single(torch, synth, dev, k)
-        M, K = w["X"].shape
-        r, L = w["B"].shape
-        ws = {op: binding.workspace(op, binding.LORA_BF16, M, K, L, r, device=dev)
-              for op in (binding.OP_FORWARD, binding.OP_BACKWARD)}
-        mw = build_multi(torch, synth, dev, k, w["X"])
-        O = sum(mw["out_slices"])
-        for op in (binding.OP_SHRINK, binding.OP_EXPAND, binding.OP_APPLY_LINEAR):
-            ws[op] = binding.workspace(op, binding.LORA_BF16, mw["T"], mw["IN"], O, mw["R"], mw["S"], device=dev)
-        sets.append(dict(w=w, mw=mw, ws=ws, M=M, K=K, L=L, r=r))
-    # embedding target: ids of the batch over a 128256-entry axis (one shared table)
-    gspec = synth.multi_spec("multi_c5", T=sets[0]["M"], IN=64, out_slices=[64], S=32)
-    gw = synth.make_multi(gspec, seed=SEED, device=dev)
-    gw["hg"] = torch.zeros((gspec["T"], gspec["R"]), dtype=torch.float32, device=dev)
-    by = single_bytes(sets[0]["M"], sets[0]["K"], sets[0]["L"], sets[0]["r"])
-    by.update(multi_bytes(sets[0]["mw"]))
-    ga = gw["ga"]
-    gslots, granks, gids = gw["slots"], gw["ranks"], gw["ids"]
-    act = [(s, i) for s, i in zip(gslots.cpu().tolist(), gids.cpu().tolist())]
-    rk = granks.cpu().tolist()
-    by["lora_gather_shrink"] = sum(rk[s] * (2 + 4) for s, i in act if 0 <= i < ga.shape[2]) + 8 * len(act)
+# ----------------------------------------------------------------------------- workloads
+def make_single_set(torch, synth, binding, dev, name, seed, prefix, peft=True):
+    spec = synth.single_spec(name)
+    w = synth.make_single(spec, seed=seed, device=dev, prefix=prefix)
+    M, K = w["X"].shape
+    r, L = w["B"].shape
+    if peft:
+        # adapter weights in the PEFT layout: lora_A.weight [r, K], lora_B.weight [L, r]
+        w["A"] = w["A"].t().contiguous().t()
+        w["B"] = w["B"].t().contiguous().t()
+    dt = binding.LORA_BF16 if spec["dtype"] == "bf16" else binding.LORA_F32
+    w["Y"] = w["Y0"].clone()
+    del w["Y0"]
+    w["dX"] = torch.empty_like(w["X"])
+    w["dA"] = torch.empty((K, r), dtype=torch.float32, device=dev)
+    w["dB"] = torch.empty((r, L), dtype=torch.float32, device=dev)
+    w["h"] = torch.empty((M, r), dtype=torch.float32, device=dev)
+    w["s"] = spec["s"]
+    w["ws"] = {op: binding.workspace(op, dt, M, K, L, r, device=dev)
+               for op in (binding.OP_FORWARD, binding.OP_BACKWARD, binding.OP_BACKWARD_DX_DA,
+                          binding.OP_BACKWARD_DB)}
+    w["dims"] = (M, K, L, r, 2 if spec["dtype"] == "bf16" else 4)
+    return w
 
-    def fwd(S):
-        w = S["w"]
-        lora.lora_forward_h(w["X"], w["A"], w["B"], w["Y"], w["s"], w["h"], ws=S["ws"][binding.OP_FORWARD])
 
-    def bwd(S):
-        w = S["w"]
+def single_fns(lora, binding):
+    def fwd(w):
+        lora.lora_forward(w["X"], w["A"], w["B"], w["Y"], w["s"], ws=w["ws"][binding.OP_FORWARD])
+
+    def fwd_h(w):
+        lora.lora_forward_h(w["X"], w["A"], w["B"], w["Y"], w["s"], w["h"], ws=w["ws"][binding.OP_FORWARD])
+
+    def bwd(w):
         lora.lora_backward(w["X"], w["dY"], w["A"], w["B"], w["h"], w["s"], w["dX"], w["dA"], w["dB"],
-                           ws=S["ws"][binding.OP_BACKWARD])
+                           ws=w["ws"][binding.OP_BACKWARD])
 
-    def shrink(S):
-        m = S["mw"]
+    def dxda(w):
+        lora.lora_backward_dx_da(w["X"], w["dY"], w["A"], w["B"], w["s"], w["dX"], w["dA"],
+                                 ws=w["ws"][binding.OP_BACKWARD_DX_DA])
+
+    def db(w):
+        lora.lora_backward_db(w["X"], w["A"], w["dY"], w["s"], w["dB"], ws=w["ws"][binding.OP_BACKWARD_DB])
+
+    return {"lora_forward": fwd, "lora_forward_h": fwd_h, "lora_backward": bwd,
+            "lora_backward_dx_da": dxda, "lora_backward_db": db}
+
+
+def make_multi_set(torch, synth, binding, dev, name, seed):
+    spec = synth.multi_spec(name)
+    w = synth.make_multi(spec, seed=seed, device=dev)
+    n, R, T = len(spec["out_slices"]), spec["R"], spec["T"]
+    O = sum(spec["out_slices"])
+    w["y"] = w["y0"].clone()
+    w["h"] = torch.zeros((T, n * R), dtype=torch.float32, device=dev)
+    w["ws"] = {op: binding.workspace(op, binding.LORA_BF16, T, w["IN"], O, R, w["S"], device=dev)
+               for op in (binding.OP_GROUP_BY_SLOT, binding.OP_SHRINK, binding.OP_EXPAND, binding.OP_APPLY_LINEAR)}
+    w["counts"] = torch.empty(w["S"], dtype=torch.int32, device=dev)
+    w["perm"] = torch.empty(max(T, 1), dtype=torch.int32, device=dev)
+    w["nact"] = torch.empty(1, dtype=torch.int32, device=dev)
+    if "ga" in w:
+        w["hg"] = torch.zeros((T, R), dtype=torch.float32, device=dev)
+    return w
+
+
+def multi_fns(lora, binding):
+    def group(m):
+        lora.lora_group_by_slot(m["slots"], m["ranks"], m["R"], m["counts"], m["perm"], m["nact"],
+                                ws=m["ws"][binding.OP_GROUP_BY_SLOT])
+
+    def shrink(m):
         lora.lora_shrink(m["x"], m["a"], m["slots"], m["ranks"], m["R"], m["h"], num_slices=len(m["out_slices"]),
-                         ws=S["ws"][binding.OP_SHRINK])
+                         ws=m["ws"][binding.OP_SHRINK])
 
-    def expand(S):
-        m = S["mw"]
+    def expand(m):
         lora.lora_expand(m["h"], m["b"], m["slots"], m["ranks"], m["scalings"], m["y"], m["out_slices"], m["R"],
-                         ws=S["ws"][binding.OP_EXPAND])
+                         ws=m["ws"][binding.OP_EXPAND])
 
-    def apply(S):
-        m = S["mw"]
+    def apply(m):
         lora.lora_apply_linear(m["x"], m["a"], m["b"], m["slots"], m["ranks"], m["scalings"], m["y"],
-                               m["out_slices"], m["R"], ws=S["ws"][binding.OP_APPLY_LINEAR])
+                               m["out_slices"], m["R"], ws=m["ws"][binding.OP_APPLY_LINEAR])
 
-    def gather(S):
-        lora.lora_gather_shrink(gids, ga, gslots, granks, gw["R"], gw["hg"])
+    def gather(m):
+        lora.lora_gather_shrink(m["ids"], m["ga"], m["slots"], m["ranks"], m["R"], m["hg"])
 
-    ops = [("lora_forward_h", fwd, by["lora_forward_h"]),
-           ("lora_backward", bwd, by["lora_backward"]),
-           ("lora_shrink", shrink, by["lora_shrink"]),
-           ("lora_expand", expand, by["lora_expand"]),
-           ("lora_apply_linear", apply, by["lora_apply_linear"]),
-           ("lora_gather_shrink", gather, by["lora_gather_shrink"])]
-    return sets, ops, sets[0]["M"]
+    return {"lora_group_by_slot": group, "lora_shrink": shrink, "lora_expand": expand,
+            "lora_apply_linear": apply, "lora_gather_shrink": gather}
+
+
+def c3_step_ops(sets, lora, binding):
+    """The headline step: (name, fn(step index), bytes) for up and down."""
+    F = single_fns(lora, binding)
+    ops = []
+    j = 0
+    for proj in ("up", "down"):
+        for op in ("lora_forward_h", "lora_backward"):
+            by = single_bytes(*sets[0][proj]["dims"])[op]
+            ops.append((f"c3_{proj}.{op}", (lambda i, proj=proj, op=op, j=j: F[op](sets[(i + j) % NSETS][proj])), by))
+            j += 1
+    return ops
 
 
 def h2d_d2h_tensors(S):
-    """(inputs copied in, results copied out) of one step, for the end-to-end leg."""
-    w, m = S["w"], S["mw"]
-    ins = [w["X"], w["Y"], w["dY"], m["y"]]
-    outs = [w["Y"], w["dX"], w["dA"], w["dB"], m["h"], m["y"]]
+    """(inputs copied in, results copied out) of one set, for the end-to-end leg."""
+    ins, outs = [], []
+    for proj in ("up", "down"):
+        w = S[proj]
+        ins += [w["X"], w["Y"], w["dY"]]
+        outs += [w["Y"], w["dX"], w["dA"], w["dB"]]
     return ins, outs
 
 
 # ----------------------------------------------------------------------------- oracle timing
-def oracle_sample(O, synth, torch, tokens):
-    """Inputs of a `tokens`-row sample of the workload, and a function that runs
-    every op of the step on them through the oracle and returns the seconds it
-    took (the gather over a 4096-entry axis: its cost per token does not depend
-    on the axis length)."""
-    spec = synth.single_spec("single_c2", M=tokens)
+def oracle_c3_sample(O, synth, torch, tokens):
+    """A `tokens`-row sample of the headline workload and a function that runs
+    its step through the fp64 oracle and returns the seconds it took."""
     gen = "cuda" if torch.cuda.is_available() else "cpu"
-    w = synth.make_single(spec, seed=SEED, device=gen, prefix="cpu")
     f = lambda t: t.double().cpu().numpy()
-    X, A, B, Y0, dY = (f(w[k]) for k in ("X", "A", "B", "Y0", "dY"))
-    ms = synth.multi_spec("multi_c4", T=tokens, IN=4096)
-    mw = synth.make_multi(ms, seed=SEED, device=gen)
-    gs = synth.multi_spec("multi_c5", T=tokens, IN=64, out_slices=[64], S=32, V=4096)
-    gw = synth.make_multi(gs, seed=SEED, device=gen)
-    sl, rk, sc = (mw[k].cpu().numpy() for k in ("slots", "ranks", "scalings"))
-    sc = sc.astype(np.float64)
-    a, b, y0 = f(mw["a"]), f(mw["b"]), f(mw["y0"])
-    ga, gsl, grk, gid = f(gw["ga"]), gw["slots"].cpu().numpy(), gw["ranks"].cpu().numpy(), gw["ids"].cpu().numpy()
-    R, osl = ms["R"], ms["out_slices"]
+    data = {}
+    for proj, name in (("up", "single_c3_up"), ("down", "single_c3_down")):
+        spec = synth.single_spec(name, M=tokens)
+        w = synth.make_single(spec, seed=SEED, device=gen, prefix="cpu_" + proj)
+        data[proj] = ({k: f(w[k]) for k in ("X", "A", "B", "Y0", "dY")}, spec["s"])
 
     def run():
         t0 = time.perf_counter()
-        O.forward(X, A, B, Y0, spec["s"])
-        O.backward_dx_da(X, dY, A, B, spec["s"])
-        O.backward_db(X, A, dY, spec["s"])
-        h = O.shrink(X, a, sl, rk, R, len(osl))
-        O.expand(h, b, sl, rk, sc, y0, osl, R)
-        O.apply_linear(X, a, b, sl, rk, sc, y0, osl, R)
-        O.gather_shrink(gid, ga, gsl, grk, gs["R"])
+        for proj in ("up", "down"):
+            d, s = data[proj]
+            O.forward(d["X"], d["A"], d["B"], d["Y0"], s)
+            O.backward_dx_da(d["X"], d["dY"], d["A"], d["B"], s)
+            O.backward_db(d["X"], d["A"], d["dY"], s)
         return time.perf_counter() - t0
 
     return run
 
 
-def cpu_baseline(torch, synth, tokens=2048, target_s=12.0, max_passes=400):
+def cpu_baseline(torch, synth, tokens=512, target_s=12.0, max_passes=400):
     """Oracle throughput on the host cores: passes over a fixed sample of the
-    workload, repeated until about `target_s` seconds of oracle work."""
+    headline workload, repeated until about `target_s` seconds of oracle work."""
     from oracle import oracle as O
     O.build()
     cores = O.num_threads()
-    run = oracle_sample(O, synth, torch, tokens)
+    run = oracle_c3_sample(O, synth, torch, tokens)
     run()   # first touch of the inputs and the library
     tot, passes = 0.0, 0
     while tot < target_s and passes < max_passes:
         tot += run()
         passes += 1
     return {"value": tokens * passes / tot, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{tokens} of the 8192 tokens through every op of the step, {passes} passes, "
-                      f"{tot:.1f} s of fp64 oracle work"}
+            "sample": f"{tokens} of the {C3_TOKENS} tokens through the up and down forward + backward, "
+                      f"{passes} passes, {tot:.1f} s of fp64 oracle work"}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -322,8 +345,8 @@ def run_reference(args, rank, world):
     from oracle import oracle as O
     O.build()
     cores = O.num_threads()
-    tokens = 256
-    run = oracle_sample(O, synth, torch, tokens)
+    tokens = 128
+    run = oracle_c3_sample(O, synth, torch, tokens)
     for _ in range(args.warmup):
         run()
     times = [run() for _ in range(args.steps)]
@@ -333,9 +356,10 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded SplitMix64)",
-            "config": {"workload": WORKLOAD, "global_batch": 8192, "seq_len": 2048, "parallelism": "replicas"},
+            "config": {"workload": WORKLOAD, "global_batch": C3_TOKENS, "parallelism": "replicas"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{tokens} of the 8192 tokens per step through every op of the step (fp64)"},
+                             "sample": f"{tokens} of the {C3_TOKENS} tokens per step through the up and down "
+                                       "forward + backward (fp64 oracle)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -356,8 +380,8 @@ def weak_scaling_value(tokens_per_rank, world, ms_per_step_max):
     return world * tokens_per_rank / (ms_per_step_max / 1e3)
 
 
-def traffic_from_profiles(kernel_key):
-    """Per-launch DRAM bytes of `kernel_key` from the committed ncu summary, if the
+def traffic_from_profiles(op_key):
+    """Per-launch DRAM bytes of `op_key` from the committed ncu summary, if the
     kernel source it was taken from is unchanged (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
@@ -367,7 +391,7 @@ def traffic_from_profiles(kernel_key):
         return None
     for parts in lines:
         kv = dict(p.split("=", 1) for p in parts if "=" in p)
-        if kv.get("op") == kernel_key:
+        if kv.get("op") == op_key:
             src = os.path.join(ROOT, kv.get("source", ""))
             try:
                 with open(src, "rb") as f:
@@ -377,6 +401,75 @@ def traffic_from_profiles(kernel_key):
             if sha == kv.get("source_sha"):
                 return int(kv["dram_bytes_per_launch"])
     return None
+
+
+def time_part(torch, stream, fn, reps, flush):
+    """Median device time (ms) of fn() over `reps` launches, L2 flushed before each."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(2):
+        flush()
+        fn(i)
+    for i in range(reps):
+        flush()
+        evs[i][0].record(stream)
+        fn(i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def run_parts(torch, lora, binding, synth, dev, stream, c3_sets, args, peak, peak_kind):
+    """Per-configuration op times, bytes and roofline fractions."""
+    which = set(args.parts.split(",")) if args.parts else {"c1", "c2", "c3", "c4", "c5"}
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.zero_()
+    reps = args.part_reps
+    SF, MF = single_fns(lora, binding), multi_fns(lora, binding)
+    out = {}
+
+    def add(cfg, op, fn, nbytes, tokens, bound="hbm"):
+        ms = time_part(torch, stream, fn, reps, flush)
+        d = {"ms": ms, "bytes": nbytes, "tokens/s": tokens / (ms / 1e3)}
+        if bound == "hbm":
+            gbs = nbytes / (ms / 1e3) / 1e9
+            d.update({"GB/s": gbs, "frac_of_" + peak_kind: gbs / peak})
+        else:
+            d["bound"] = bound
+        out[f"{cfg}.{op}"] = d
+
+    if "c1" in which:
+        w = make_single_set(torch, synth, binding, dev, "single_c1", SEED, "part_c1", peft=False)
+        by = single_bytes(*w["dims"])
+        for op in ("lora_forward", "lora_backward_dx_da", "lora_backward_db"):
+            add("c1", op, lambda i, op=op: SF[op](w), by[op], w["dims"][0], bound="launch")
+        del w
+    if "c2" in which:
+        w = make_single_set(torch, synth, binding, dev, "single_c2", SEED, "part_c2")
+        by = single_bytes(*w["dims"])
+        for op in ("lora_forward", "lora_backward_dx_da", "lora_backward_db", "lora_forward_h", "lora_backward"):
+            add("c2", op, lambda i, op=op: SF[op](w), by[op], w["dims"][0])
+        del w
+    if "c3" in which:
+        for proj in ("up", "down"):
+            by = single_bytes(*c3_sets[0][proj]["dims"])
+            for op in ("lora_forward_h", "lora_backward"):
+                add(f"c3_{proj}", op, lambda i, op=op, proj=proj: SF[op](c3_sets[i % NSETS][proj]), by[op],
+                    C3_TOKENS)
+    for cfg, name in (("c4", "multi_c4"), ("c5", "multi_c5")):
+        if cfg not in which:
+            continue
+        m = make_multi_set(torch, synth, binding, dev, name, SEED)
+        by = multi_bytes(m)
+        ops = ["lora_group_by_slot", "lora_shrink", "lora_expand", "lora_apply_linear"]
+        if "ga" in m:
+            ops.append("lora_gather_shrink")
+        for op in ops:
+            lat = op in ("lora_group_by_slot", "lora_gather_shrink")
+            add(cfg, op, lambda i, op=op: MF[op](m), by[op], m["T"], bound="latency" if lat else "hbm")
+        del m
+    del flush_buf
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_gb300(args, rank, world, local_rank):
@@ -395,22 +488,17 @@ def run_gb300(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.current_stream()
-    sets, ops, tokens = make_ops(torch, lora, binding, synth, dev)
-    if args.only:
-        # names with or without the "lora_" prefix
-        keep = {k if k.startswith("lora_") else "lora_" + k for k in args.only.split(",")}
-        unknown = keep - {op[0] for op in ops}
-        if unknown:
-            raise SystemExit(f"--only: unknown op(s) {sorted(unknown)}; known: {[op[0] for op in ops]}")
-        ops = [op for op in ops if op[0] in keep]
+    sets = [{proj: make_single_set(torch, synth, binding, dev, f"single_c3_{proj}", SEED + k, f"bench{k}_{proj}")
+             for proj in ("up", "down")} for k in range(NSETS)]
+    ops = c3_step_ops(sets, lora, binding)
+    tokens = C3_TOKENS
     torch.cuda.synchronize()
 
     def step(i, events=None):
         for j, (name, fn, _) in enumerate(ops):
-            S = sets[(i + j) % NSETS]
             if events is not None:
                 events[j][0].record(stream)
-            fn(S)
+            fn(i)
             if events is not None:
                 events[j][1].record(stream)
 
@@ -485,8 +573,8 @@ def run_gb300(args, rank, world, local_rank):
     ms_per_step = ms / K
     value = weak_scaling_value(tokens, world, ms_per_step)
 
-    # per-op device times (eager launches, events around each op, same rotation)
-    KP = max(10, min(K, 200))
+    # per-op device times inside the step (eager launches, events around each op, same rotation)
+    KP = max(10, min(K, 50))
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
            for _ in range(KP)]
     for i in range(KP):
@@ -494,16 +582,17 @@ def run_gb300(args, rank, world, local_rank):
     torch.cuda.synchronize()
 
     peak, peak_kind = peaks()
-    parts = {}
+    step_parts = {}
     for j, (name, _, nbytes) in enumerate(ops):
         t_ms = statistics.mean(evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(KP))
         gbs = nbytes / (t_ms / 1e3) / 1e9
-        parts[name] = {"ms": t_ms, "bytes": nbytes, "GB/s": gbs, "frac_of_" + peak_kind: gbs / peak,
-                       "tokens/s": tokens / (t_ms / 1e3)}
-    dom = max(parts, key=lambda n: parts[n]["ms"])
-    roof = {"bound": "hbm", "op": dom, "achieved": parts[dom]["GB/s"], "peak": peak, "unit": "GB/s",
-            "frac": parts[dom]["GB/s"] / peak, "peak_kind": peak_kind,
-            "traffic": traffic_from_profiles(dom), "bytes_per_launch": parts[dom]["bytes"]}
+        step_parts[name] = {"ms": t_ms, "bytes": nbytes, "GB/s": gbs, "frac_of_" + peak_kind: gbs / peak,
+                            "tokens/s": tokens / (t_ms / 1e3)}
+    dom = max(step_parts, key=lambda n: step_parts[n]["ms"])
+    roof = {"bound": "hbm", "op": dom, "achieved": step_parts[dom]["GB/s"], "peak": peak, "unit": "GB/s",
+            "frac": step_parts[dom]["GB/s"] / peak, "peak_kind": peak_kind,
+            "traffic": traffic_from_profiles(dom), "bytes_per_launch": step_parts[dom]["bytes"]}
+    step_bytes = sum(p["bytes"] for p in step_parts.values())
 
     # end to end: pinned host inputs in, results out, every step
     E = min(args.e2e_steps, K)
@@ -511,20 +600,20 @@ def run_gb300(args, rank, world, local_rank):
                for S in sets]
     host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in h2d_d2h_tensors(S)[1]]
                 for S in sets]
-    h2d = sum(t.numel() * t.element_size() for t in host_in[0])
-    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    used = sorted({(0 + j) % NSETS for j in range(len(ops))})
 
     def e2e_step(i):
-        S_i = [(i + j) % NSETS for j in range(len(ops))]
-        for k in sorted(set(S_i)):
+        ks = sorted({(i + j) % NSETS for j in range(len(ops))})
+        for k in ks:
             for dst, src in zip(h2d_d2h_tensors(sets[k])[0], host_in[k]):
                 dst.copy_(src, non_blocking=True)
         step(i)
-        for k in sorted(set(S_i)):
+        for k in ks:
             for dst, src in zip(host_out[k], h2d_d2h_tensors(sets[k])[1]):
                 dst.copy_(src, non_blocking=True)
 
-    sets_per_step = len({(0 + j) % NSETS for j in range(len(ops))})
+    h2d = sum(t.numel() * t.element_size() for k in used for t in host_in[k])
+    d2h = sum(t.numel() * t.element_size() for k in used for t in host_out[k])
     e_ms = None
     if E > 0:
         for i in range(2):
@@ -538,7 +627,13 @@ def run_gb300(args, rank, world, local_rank):
         f1.record(stream)
         torch.cuda.synchronize()
         e_ms = reduce_max(f0.elapsed_time(f1) / E, dev)
+    del host_in, host_out
     assert lora.lora_device_error() == 0
+
+    parts = None
+    if not args.no_parts:
+        parts = run_parts(torch, lora, binding, synth, dev, stream, sets, args, peak, peak_kind)
+        assert lora.lora_device_error() == 0
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -549,14 +644,16 @@ def run_gb300(args, rank, world, local_rank):
                 "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic (seeded SplitMix64; inputs resident in HBM)",
-                "config": {"workload": WORKLOAD, "model": "q_proj LoRA (Llama-like 4096)", "global_batch": 8192 * world,
-                           "seq_len": 2048, "parallelism": f"replicas x{world}",
-                           "l2": f"{NSETS} rotating input sets, each > L2; consecutive ops use different sets",
-                           "launch": "eager" if graphs is None else "CUDA graph per step (PDL edges kept)"},
-                "parts": parts, "roofline": roof, "cpu_baseline": cpu,
+                "config": {"workload": WORKLOAD, "model": "Llama-like MLP (4096 <-> 14336) LoRA r=64",
+                           "global_batch": C3_TOKENS * world, "parallelism": f"replicas x{world}",
+                           "l2": f"{NSETS} rotating input sets; every operand > L2; consecutive ops use "
+                                 "different sets",
+                           "launch": "eager" if graphs is None else "CUDA graph per step (PDL edges kept)",
+                           "step_bytes": step_bytes},
+                "step_parts": step_parts, "parts": parts, "roofline": roof, "cpu_baseline": cpu,
                 "e2e": None if e_ms is None else {
                     "value": weak_scaling_value(tokens, world, e_ms), "unit": UNIT, "steps": E,
-                    "h2d_bytes_per_step": h2d * sets_per_step, "d2h_bytes_per_step": d2h * sets_per_step},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": int(launches), "clocks": sampler.summary(t_host0, t_host1)}
         print(json.dumps(line), flush=True)
 

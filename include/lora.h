@@ -235,9 +235,14 @@ LORA_API lora_status_t lora_backward_db(lora_dtype_t dtype, int64_t M, int64_t K
  *   until the process exits.  Sizes whose lora_workspace_size(LORA_OP_BACKWARD_DB,
  *   ...) exceeds it are rejected with LORA_ERR_WORKSPACE before anything is
  *   launched.  No cudaMalloc, cudaFree or allocating library call is made.
- *   The first call on a device looks up the array's device address on that
- *   device (the device current at the call); make that first call before any
- *   stream capture.  All calls share the one array and the kernels re-clear what
+ *   Argument errors (dtype, negative or oversized extents, rank) are reported
+ *   before the size check.  The first call in a CUDA context (for runtime-API
+ *   callers the primary context of the current device; else the context current
+ *   on the calling thread) looks up the array's device address in that context
+ *   and caches it under the context's unique id, so a context created later
+ *   (after cudaDeviceReset, or by an engine's own cuCtxCreate) gets its own
+ *   lookup.  Make that first call before any stream capture in that context.
+ *   All calls share the one array and the kernels re-clear what
  *   must start at zero on every call, but two calls that can run at the same time
  *   on the GPU (other streams, other host threads) race on it: serialise them.
  * -------------------------------------------------------------------------------- */

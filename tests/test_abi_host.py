@@ -132,3 +132,18 @@ def test_multi_argument_errors(L):
     assert L.lora_gather_shrink(P(ad), FAKE, 100, NULL, FAKE, 800, 100, 1, FAKE, 8, S0) == 1
     empty = B.LoraAddressing(0, 0, 4, 8)
     assert L.lora_gather_shrink(P(empty), NULL, 100, NULL, NULL, 800, 100, 1, NULL, 8, S0) == 0
+
+
+def test_noalloc_argument_errors_come_before_the_size_check(L):
+    """lora_backward_db_noalloc reports a bad dtype, size or rank as such (the
+    errors of lora_backward_db), and only then compares the workspace the call
+    would need with its fixed scratch array; nothing is launched either way."""
+    M, K, Lc, r = 16384, 14336, 4096, 64
+    scratch = 16 << 20
+    assert L.lora_workspace_size(B.OP_BACKWARD_DB, B.LORA_BF16, M, K, Lc, r, 0) > scratch
+    nb = lambda dt=B.LORA_BF16, m=M, rr=r: L.lora_backward_db_noalloc(
+        dt, m, K, Lc, rr, FAKE, K, FAKE, 1, K, FAKE, Lc, 0.5, FAKE, Lc, 1, S0)
+    assert nb(dt=7) == 2                  # unsupported dtype, not a scratch overflow
+    assert nb(m=-1) == 1                  # negative size
+    assert nb(rr=500) == 2                # rank above LORA_MAX_RANK
+    assert nb() == 4                      # valid but larger than the scratch array
