@@ -6,7 +6,7 @@
 //   apply_linear_  shrink then expand into y
 //   gather_shrink  h[t] = a[slot(t)][:, ids[t]]  (ids outside [0, V) give zeros)
 // and the integer step in front of them (group_by_slot): a stable counting sort
-// of the active tokens by slot and a list of tiles of at most 64 tokens of one
+// of the active tokens by slot and a list of tiles of at most 128 tokens of one
 // slot, built on the device with no host sync (the page requires the ops to run
 // without one).
 //
@@ -872,7 +872,10 @@ lora_status_t launch_group(const lora_addressing_t &ad, const int32_t *ranks, in
                            int32_t *num_active, int *header, int4 *tiles, cudaStream_t st) {
   const int S = ad.num_slots;
   int nw = (int)std::max<int64_t>(1, (160 * 1024 / 4 - 256 - 3 * S) / S);   // shared-memory bound
-  nw = std::min<int64_t>({nw, 32, std::max<int64_t>(1, ceil_div(ad.num_tokens, LORA_GROUP_TOKENS_PER_WARP))});
+  // enough warps for the tokens, and for the per-slot scans (a warp scans the
+  // slots s = w, w + nw, ...): at most 8 slots per warp
+  const int64_t want = std::max<int64_t>(ceil_div(ad.num_tokens, LORA_GROUP_TOKENS_PER_WARP), ceil_div(S, 8));
+  nw = std::min<int64_t>({nw, 32, std::max<int64_t>(1, want)});
   const size_t smem = (size_t)(nw * S + 3 * S + 160) * 4;
   LORA_CUDA(ensure_smem((const void *)group_kernel, smem));
   LORA_CUDA(launch(group_kernel, dim3(1), dim3(nw * 32), smem, st, 1, true, ad.slots, ad.num_tokens, S,

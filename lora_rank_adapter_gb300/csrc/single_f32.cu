@@ -13,7 +13,7 @@
 
 namespace lora {
 
-constexpr int kF32Rows = 16;
+constexpr int kF32Rows = 2;   // rows per block of the forward (more blocks in flight)
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -32,10 +32,20 @@ __global__ void __launch_bounds__(256) fwd_f32_kernel(SingleArgs a) {
   for (int pr = warp; pr < kF32Rows * a.r; pr += nw) {
     const int row = pr / a.r, j = pr % a.r;
     const int64_t m = m0 + row;
-    float acc = 0.f;
-    if (m < a.M)
-      for (int64_t k = lane; k < a.K; k += 32) acc += X[m * a.ldx + k] * A[k * a.sA_k + j * a.sA_r];
-    acc = warp_sum(acc);
+    // four independent partial sums per lane keep four loads in flight
+    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+    if (m < a.M) {
+      const float *xr = X + m * a.ldx, *ac = A + j * a.sA_r;
+      int64_t k = lane;
+      for (; k + 96 < a.K; k += 128) {
+        p0 += xr[k] * ac[k * a.sA_k];
+        p1 += xr[k + 32] * ac[(k + 32) * a.sA_k];
+        p2 += xr[k + 64] * ac[(k + 64) * a.sA_k];
+        p3 += xr[k + 96] * ac[(k + 96) * a.sA_k];
+      }
+      for (; k < a.K; k += 32) p0 += xr[k] * ac[k * a.sA_k];
+    }
+    const float acc = warp_sum((p0 + p1) + (p2 + p3));
     if (lane == 0) {
       h[row * a.r + j] = acc;
       if (a.h != nullptr && m < a.M) a.h[m * a.ldh + j] = acc;   // lora_forward_h
