@@ -13,6 +13,7 @@
 #include "host_common.h"
 #include "multi.h"
 #include "single_bf16.h"
+#include "single_tc.h"
 
 namespace lora {
 
@@ -128,21 +129,13 @@ static lora_status_t check_single_common(lora_dtype_t dt, int64_t M, int64_t K, 
 }
 
 static size_t single_ws(int op, lora_dtype_t dt, int64_t M, int64_t K, int64_t L, int r) {
-  return dt == LORA_BF16 ? bf16_ws_bytes(op, M, K, L, r) : f32_ws_bytes(op, M, K, L, r);
+  return dt == LORA_BF16 ? tc_ws_bytes(op, M, K, L, r) : f32_ws_bytes(op, M, K, L, r);
 }
 
 // Workspace the call will actually use (packing only when a layout needs it).
 static size_t single_ws_needed(int op, const SingleArgs &a) {
   if (a.dtype != LORA_BF16) return f32_ws_bytes(op, a.M, a.K, a.L, a.r);
-  size_t full = bf16_ws_bytes(op, a.M, a.K, a.L, a.r);
-  if (op == LORA_OP_FORWARD) {
-    SingleLayout lay = plan_layout(a, true, a.L > 0);
-    size_t n = 0;
-    if (lay.pack_A) n += ws_round((size_t)a.r * round_up(a.K, 8) * 2);
-    if (lay.pack_B) n += ws_round((size_t)a.L * round_up(a.r, 8) * 2);
-    return n;
-  }
-  return full;
+  return tc_ws_bytes(op, a.M, a.K, a.L, a.r);
 }
 
 }  // namespace lora
@@ -207,7 +200,7 @@ lora_status_t lora_forward(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, 
   a.Y = Y; a.ldy = ldy; a.scale = scale;
   LORA_TRY(check_ws(ws, ws_bytes, single_ws_needed(LORA_OP_FORWARD, a)));
   cudaStream_t st = (cudaStream_t)stream;
-  return dtype == LORA_BF16 ? forward_bf16(a, ws, ws_bytes, st) : forward_f32(a, st);
+  return dtype == LORA_BF16 ? forward_tc(a, ws, ws_bytes, st) : forward_f32(a, st);
 }
 
 lora_status_t lora_forward_h(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r, const void *X,
@@ -228,7 +221,7 @@ lora_status_t lora_forward_h(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L
   a.X = X; a.ldx = ldx; a.A = A; a.sA_k = sA_k; a.sA_r = sA_r; a.B = B; a.sB_r = sB_r; a.sB_l = sB_l;
   a.Y = Y; a.ldy = ldy; a.scale = scale; a.h = h; a.ldh = ldh;
   LORA_TRY(check_ws(ws, ws_bytes, single_ws_needed(LORA_OP_FORWARD, a)));
-  return dtype == LORA_BF16 ? forward_bf16(a, ws, ws_bytes, st) : forward_f32(a, st);
+  return dtype == LORA_BF16 ? forward_tc(a, ws, ws_bytes, st) : forward_f32(a, st);
 }
 
 lora_status_t lora_backward_ex(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r, const void *X,
@@ -267,7 +260,7 @@ lora_status_t lora_backward_ex(lora_dtype_t dtype, int64_t M, int64_t K, int64_t
   a.dx_acc = acc ? 1 : 0;
   a.grad_lo = gdt == LORA_BF16 ? 1 : 0;
   LORA_TRY(check_ws(ws, ws_bytes, single_ws_needed(LORA_OP_BACKWARD, a)));
-  return dtype == LORA_BF16 ? backward_bf16(a, ws, ws_bytes, st) : backward_f32(a, ws, ws_bytes, st);
+  return dtype == LORA_BF16 ? backward_tc(a, ws, ws_bytes, st) : backward_f32(a, ws, ws_bytes, st);
 }
 
 lora_status_t lora_backward(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r, const void *X, int64_t ldx,
@@ -304,7 +297,7 @@ lora_status_t lora_backward_dx_da(lora_dtype_t dtype, int64_t M, int64_t K, int6
   a.B = B; a.sB_r = sB_r; a.sB_l = sB_l; a.scale = scale; a.dX = dX; a.lddx = lddx;
   a.dA = dA; a.sdA_k = sdA_k; a.sdA_r = sdA_r;
   LORA_TRY(check_ws(ws, ws_bytes, single_ws_needed(LORA_OP_BACKWARD_DX_DA, a)));
-  return dtype == LORA_BF16 ? backward_dx_da_bf16(a, ws, ws_bytes, st) : backward_dx_da_f32(a, ws, ws_bytes, st);
+  return dtype == LORA_BF16 ? backward_dx_da_tc(a, ws, ws_bytes, st) : backward_dx_da_f32(a, ws, ws_bytes, st);
 }
 
 lora_status_t lora_backward_db(lora_dtype_t dtype, int64_t M, int64_t K, int64_t L, int32_t r, const void *X,
@@ -327,7 +320,7 @@ lora_status_t lora_backward_db(lora_dtype_t dtype, int64_t M, int64_t K, int64_t
   a.X = X; a.ldx = ldx; a.A = A; a.sA_k = sA_k; a.sA_r = sA_r; a.dY = dY; a.lddy = lddy;
   a.scale = scale; a.dB = dB; a.sdB_r = sdB_r; a.sdB_l = sdB_l;
   LORA_TRY(check_ws(ws, ws_bytes, single_ws_needed(LORA_OP_BACKWARD_DB, a)));
-  return dtype == LORA_BF16 ? backward_db_bf16(a, ws, ws_bytes, st) : backward_db_f32(a, ws, ws_bytes, st);
+  return dtype == LORA_BF16 ? backward_db_tc(a, ws, ws_bytes, st) : backward_db_f32(a, ws, ws_bytes, st);
 }
 
 // ----------------------------------------------------------------------------- multi adapter
@@ -446,7 +439,8 @@ lora_status_t lora_gather_shrink(const lora_addressing_t *addr, const int32_t *r
 lora_status_t lora_device_error(int32_t *code) {
   if (code == nullptr) return LORA_ERR_INVALID_ARG;
   int v = 0;
-  int parts[3] = {read_clear_error_single_bf16(), read_clear_error_single_f32(), read_clear_error_multi()};
+  int parts[4] = {read_clear_error_single_bf16(), read_clear_error_single_f32(), read_clear_error_multi(),
+                  read_clear_error_single_tc()};
   for (int p : parts) {
     if (p < 0) return LORA_ERR_CUDA;
     v |= p;

@@ -917,6 +917,16 @@ __global__ void pack2d_bf16_kernel(const __nv_bfloat16 *src, int64_t s_row, int6
 }
 
 // ----------------------------------------------------------------------------- host side
+lora_status_t pack_bf16_2d(const void *src, int64_t s_row, int64_t s_col, int64_t rows, int64_t cols, void *dst,
+                           int64_t ldd, cudaStream_t st) {
+  const int64_t n = rows * cols;
+  int blocks = (int)std::min<int64_t>(ceil_div(n, 256), 4 * num_sms());
+  if (blocks < 1) blocks = 1;
+  LORA_CUDA(launch(pack2d_bf16_kernel, dim3(blocks), dim3(256), 0, st, 1, true, (const __nv_bfloat16 *)src, s_row,
+                   s_col, (int)rows, (int)cols, (__nv_bfloat16 *)dst, ldd));
+  return LORA_OK;
+}
+
 namespace {
 
 CUtensorMapSwizzle swz_for(int row_bytes) {

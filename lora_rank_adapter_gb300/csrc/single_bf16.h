@@ -79,6 +79,10 @@ lora_status_t backward_dx_da_f32(const SingleArgs &a, void *ws, size_t ws_bytes,
 lora_status_t backward_db_f32(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
 lora_status_t backward_f32(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
 
+// Strided 2-D bf16 copy into a dense [rows][ldd] layout (repacking A or B).
+lora_status_t pack_bf16_2d(const void *src, int64_t s_row, int64_t s_col, int64_t rows, int64_t cols, void *dst,
+                           int64_t ldd, cudaStream_t st);
+
 // Zero fills used for degenerate shapes (outputs defined as overwritten).
 lora_status_t fill_zero_2d(lora_dtype_t dt, void *p, int64_t rows, int64_t cols, int64_t s_row, int64_t s_col,
                            cudaStream_t st);

@@ -1,0 +1,1064 @@
+// single_tc.cu -- single-adapter LoRA kernels (bf16 storage, fp32 accumulation)
+// on the fifth-generation tensor cores of sm_103a: tcgen05.mma with the
+// accumulators in tensor memory (TMEM), operands staged in shared memory by the
+// tensor-memory accelerator (TMA).
+//
+// Operations ([NeMo lora_kernel] = NeMo AutoModel API page
+// "nemo_automodel.components._peft.lora_kernel"), in forward roles X [M,K],
+// A [K,r], B [r,L]:
+//   forward   Y += s * (X*A)*B       lora_forward_kernel (inner_kernel, block_vector_mul)
+//   dyb       dY * B^T                lora_da_dx_kernel (DYB = DY x B)
+//   dX, dA    s * dyb*A^T, s * X^T*dyb   lora_da_dx_kernel / lora_da_dx_update_wrapper
+//   h, dB     X*A, s * h^T*dY           lora_db_kernel / lora_db_update_wrapper
+//
+// Three kernels do all of it:
+//   rows_kernel    out[m, :] = In[m, :] * W over a contraction of C columns, for
+//                  128-row blocks (h = X*A with W = A, dyb = dY*B^T with W = B^T).
+//                  The (row block, 64-column chunk) units are split evenly over a
+//                  persistent grid (stream-K); a row block cut between CTAs leaves
+//                  fp32 partial sums in the workspace and the last CTA to finish
+//                  adds them in CTA order (deterministic).  The result goes out as
+//                  a "blob": the bf16 hi and lo parts (v ~= hi + lo to ~2^-17) of
+//                  the 128 x RP block, already in the swizzled layout the tensor
+//                  cores read, and optionally as fp32 rows (the saved h).
+//   expand_kernel  Y[m, l] += s * sum_j h[m, j] B[j, l] over (row block, 64-column
+//                  chunk of Y) units: h hi/lo from the blob, B^T chunks and Y tiles
+//                  by TMA, the product in TMEM, Y read-modify-written once.
+//   col_kernel     acc[c, :] = sum over rows m of In[m, c] * blob[m, :] for
+//                  128-column blocks of In (dA = X^T*dyb, dB^T = dY^T*h), stream-K
+//                  over (column block, 128-row tile) units with the same ordered
+//                  reduction; with kDX it also writes, per row tile, the dX tile
+//                  s * dyb*A^T (dX is read-modified-written when accumulating).
+// Warp roles in every kernel: warp 0 loads (one lane issues TMA), warp 1 issues
+// the MMAs (one lane) and owns the TMEM allocation, warps 2..5 drain TMEM (one
+// accumulator row per thread; warp w reads TMEM lanes 32 (w % 4) ..).
+//
+// Operand layouts: every staged tile is rows of 32/64/128 bytes with the
+// matching TMA swizzle.  A tile is read K-major (rows = M or N, K along the row)
+// or MN-major (rows = K, M or N along the row); the second form lets the
+// transposed products (X^T, dY^T, B^T in PEFT layout) use the tiles as TMA
+// wrote them.
+#include <algorithm>
+#include <type_traits>
+
+#include "common.cuh"
+#include "host_common.h"
+#include "single_bf16.h"
+#include "single_tc.h"
+
+namespace lora {
+namespace tc {
+
+constexpr int TM = 128;        // rows of a tile (the MMA M)
+constexpr int BOXC = 64;       // columns of one TMA box (128 bytes of bf16)
+constexpr int NTHR = 192;      // six warps
+constexpr int EPI0 = 2;        // first epilogue warp
+constexpr int kRingBytes = 196 * 1024;
+
+__host__ __device__ constexpr int pw_of(int RP) { return RP < 64 ? RP : 64; }
+// bytes of one (hi or lo) 128 x RP bf16 tile of a blob
+__host__ __device__ constexpr int blob_tile(int RP) { return TM * RP * 2; }
+__host__ __device__ constexpr int tmem_cols(int need) {
+  return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
+}
+
+// Byte offset of (row, col) in a blob tile: panels of PW columns, each [128][PW]
+// with a (2 PW)-byte swizzle.
+template <int RP>
+__device__ __forceinline__ uint32_t blob_off(int row, int col) {
+  constexpr int PW = pw_of(RP);
+  return (uint32_t)((col / PW) * (TM * PW * 2)) + swz((uint32_t)row, (uint32_t)(col % PW) * 2, PW * 2);
+}
+
+// ----------------------------------------------------------------------------- stream-K split
+// Units [0, U) are dealt to G CTAs in contiguous runs: CTA i takes [b(i), b(i+1)).
+__host__ __device__ __forceinline__ int64_t sk_begin(int64_t U, int G, int i) { return U * i / G; }
+// The CTA whose run holds unit u.
+__host__ __device__ __forceinline__ int sk_cta(int64_t U, int G, int64_t u) {
+  int i = (int)(u * G / U);
+  while (i + 1 < G && sk_begin(U, G, i + 1) <= u) ++i;
+  while (i > 0 && sk_begin(U, G, i) > u) --i;
+  return i;
+}
+
+__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+template <int RP>
+__device__ __forceinline__ void store_partial(float *part, int row, const float *v) {
+  float4 *p = reinterpret_cast<float4 *>(part + (int64_t)row * RP);
+#pragma unroll
+  for (int j = 0; j < RP / 4; ++j) __stcg(p + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+}
+// RP accumulator columns of this thread's TMEM lane.
+template <int RP>
+__device__ __forceinline__ void tmem_row(uint32_t taddr, float *v) {
+  if constexpr (RP == 16) {
+    float t[16];
+    tmem_ld16(taddr, t);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = t[j];
+  } else {
+#pragma unroll
+    for (int c = 0; c < RP; c += 32) tmem_ld32(taddr + c, v + c);
+  }
+}
+
+// Partial sums live per CTA: a CTA's run meets a group that it does not cover
+// whole only as its first group (slot 0) or its last group (slot 1).
+__host__ __device__ __forceinline__ int64_t part_slot(int64_t U, int G, int c, int64_t g, int64_t n) {
+  return 2 * (int64_t)c + (sk_begin(U, G, c) / n == g ? 0 : 1);
+}
+
+// The epilogue's end of the segment of group g (units [g n, (g + 1) n)) that CTA
+// i computed: either the group is all this CTA's (no partial), or the partial
+// goes to the workspace and the last CTA of the group to finish adds the
+// partials of all its CTAs in CTA order.  Returns true when this CTA then holds
+// the group's full sum in v.  Called by the four epilogue warps together.
+template <int RP>
+__device__ __forceinline__ bool reduce_segment(int64_t U, int G, int i, int64_t g, int64_t n, float *part,
+                                               int *counter, int row, float *v, int *s_flag) {
+  const int first = sk_cta(U, G, g * n), last_cta = sk_cta(U, G, (g + 1) * n - 1);
+  if (first == last_cta) return true;
+  store_partial<RP>(part + part_slot(U, G, i, g, n) * TM * RP, row, v);
+  __threadfence();
+  named_bar_sync(1, 128);
+  if (threadIdx.x == EPI0 * 32) *s_flag = atomicAdd(counter, 1) == last_cta - first;
+  named_bar_sync(1, 128);
+  const bool last = *s_flag != 0;
+  if (last) {
+    __threadfence();
+#pragma unroll
+    for (int j = 0; j < RP; ++j) v[j] = 0.f;
+    for (int c = first; c <= last_cta; ++c) {
+      const float4 *p4 = reinterpret_cast<const float4 *>(part + (part_slot(U, G, c, g, n) * TM + row) * RP);
+#pragma unroll
+      for (int j = 0; j < RP / 4; ++j) {
+        const float4 t = __ldcg(p4 + j);
+        v[4 * j] += t.x;
+        v[4 * j + 1] += t.y;
+        v[4 * j + 2] += t.z;
+        v[4 * j + 3] += t.w;
+      }
+    }
+    if (threadIdx.x == EPI0 * 32) *counter = 0;   // ready for the next call
+  }
+  named_bar_sync(1, 128);   // s_flag is reused by the next segment
+  return last;
+}
+
+// ============================================================================= rows
+template <int RP, bool kWMN>
+struct RowsCfg {
+  static constexpr int PW = pw_of(RP);
+  static constexpr int IN_B = TM * BOXC * 2;    // 16 KB
+  static constexpr int W_B = RP * 128;          // Ac [RP][64] or B^T [64][RP]
+  static constexpr int STAGE = IN_B + W_B;
+  static constexpr int NS = kRingBytes / STAGE > 8 ? 8 : kRingBytes / STAGE;
+  static constexpr int TMEM = tmem_cols(2 * RP);
+  static constexpr int BYTES = 1024 + NS * STAGE + 1024;
+};
+
+template <int RP, bool kWMN>
+__global__ void __launch_bounds__(NTHR, 1) rows_kernel(const __grid_constant__ CUtensorMap tmIn,
+                                                       const __grid_constant__ CUtensorMap tmW, TcRowsArgs p) {
+  using C = RowsCfg<RP, kWMN>;
+  constexpr int NS = C::NS, PW = C::PW;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(ring + NS * C::STAGE);
+  uint64_t *empty = full + NS;
+  uint64_t *afull = empty + NS;    // [2] accumulator written
+  uint64_t *aempty = afull + 2;    // [2] accumulator drained
+  uint64_t *mdone = aempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mdone + 1);
+  int *s_flag = reinterpret_cast<int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x;
+  const int64_t u0 = sk_begin(p.U, p.G, i), u1 = sk_begin(p.U, p.G, i + 1);
+  const int nc = p.nc;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&afull[b], 1);
+      mbar_init(&aempty[b], 4);
+    }
+    mbar_init(mdone, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ loader
+    if (lane == 0) {
+      prefetch_tmap(&tmIn);
+      prefetch_tmap(&tmW);
+      for (int64_t u = u0; u < u1; ++u) {
+        const int g = (int)(u - u0), s = g % NS;
+        if (g >= NS && !mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) break;
+        const int rb = (int)(u / nc), c = (int)(u % nc);
+        uint8_t *st = ring + s * C::STAGE;
+        mbar_arrive_expect_tx(&full[s], C::STAGE);
+        tma_load_2d(st, &tmIn, &full[s], c * BOXC, rb * TM);
+        if (kWMN) {
+#pragma unroll
+          for (int pp = 0; pp < RP / PW; ++pp)
+            tma_load_2d(st + C::IN_B + pp * (BOXC * PW * 2), &tmW, &full[s], pp * PW, c * BOXC);
+        } else {
+          tma_load_2d(st + C::IN_B, &tmW, &full[s], c * BOXC, 0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = tc_idesc(TM, RP, false, kWMN);
+      int seg = 0;
+      bool ok = true;
+      for (int64_t u = u0; ok && u < u1; ++u) {
+        const int g = (int)(u - u0), s = g % NS;
+        const int c = (int)(u % nc);
+        const bool first = u == u0 || c == 0, last = u == u1 - 1 || c == nc - 1;
+        const int b = seg & 1;
+        if (first && seg >= 2 && !(ok = mbar_wait(&aempty[b], ((seg >> 1) & 1) ^ 1))) break;
+        if (!(ok = mbar_wait(&full[s], (g / NS) & 1))) break;
+        tc_fence_after();
+        const uint32_t st = smem_u32(ring + s * C::STAGE), w = st + C::IN_B;
+#pragma unroll
+        for (int kk = 0; kk < BOXC / 16; ++kk) {
+          const uint64_t ad = tc_desc(st + kk * 32, 16, 1024, 128);
+          const uint64_t bd = kWMN ? tc_desc(w + kk * 16 * PW * 2, RP > PW ? BOXC * PW * 2 : 16, 8 * PW * 2, PW * 2)
+                                   : tc_desc(w + kk * 32, 16, 1024, 128);
+          tc_mma_bf16(tmem + b * RP, ad, bd, idesc, (first && kk == 0) ? 0u : 1u);
+        }
+        tc_commit(&empty[s]);
+        if (last) {
+          tc_commit(&afull[b]);
+          ++seg;
+        }
+      }
+      tc_commit(mdone);
+      mbar_wait(mdone, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3, row = 32 * q + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+    float v[RP];
+    int seg = 0;
+    bool ok = true;   // after a timed-out wait: skip the work, keep the barrier sequence
+    const int64_t rb0 = u0 < u1 ? u0 / nc : 0, rb1 = u0 < u1 ? (u1 - 1) / nc : -1;
+    for (int64_t rb = rb0; rb <= rb1; ++rb, ++seg) {
+      const int b = seg & 1;
+      if (ok) ok = wait_warp(&afull[b], (seg >> 1) & 1);
+#pragma unroll
+      for (int j = 0; j < RP; ++j) v[j] = 0.f;
+      if (ok) {
+        tc_fence_after();
+        tmem_row<RP>(tl + b * RP, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&aempty[b]);
+      }
+      if (!reduce_segment<RP>(p.U, p.G, i, rb, nc, p.part, p.counters + rb, row, v, s_flag)) continue;
+      // the block's full sum: the hi / lo blob, and the fp32 rows when asked for
+      uint8_t *bhi = p.blob + rb * (int64_t)(2 * blob_tile(RP)), *blo = bhi + blob_tile(RP);
+#pragma unroll
+      for (int j = 0; j < RP; j += 8) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split_bf16(v[j + 2 * e], v[j + 2 * e + 1], hi[e], lo[e]);
+        const uint32_t o = blob_off<RP>(row, j);
+        *reinterpret_cast<uint4 *>(bhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(blo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      const int64_t grow = rb * TM + row;
+      if (p.hout != nullptr && grow < p.M) {
+        float *hr = p.hout + grow * p.ldh;
+#pragma unroll
+        for (int j = 0; j < RP; ++j)
+          if (j < p.r) hr[j] = v[j];
+      }
+    }
+  }
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM);
+  }
+}
+
+// ============================================================================= expand
+// Y[m, l] += s * (h_hi + h_lo)[m, :] . B^T[l, :]; four TMEM accumulators of 64
+// columns let the epilogue of one chunk overlap the MMAs of the next.
+template <int RP>
+struct ExpCfg {
+  static constexpr int PW = pw_of(RP);
+  static constexpr int Y_B = TM * BOXC * 2;      // 16 KB
+  static constexpr int B_B = BOXC * RP * 2;      // B^T chunk [64 l][RP]
+  static constexpr int STAGE = Y_B + B_B;
+  static constexpr int HB = 2 * blob_tile(RP);   // hi + lo of one row block
+  static constexpr int NS0 = (kRingBytes - 2 * HB) / STAGE;
+  static constexpr int NS = NS0 > 8 ? 8 : NS0;
+  static constexpr int ND = 4;
+  static constexpr int TMEM = 256;
+  static constexpr int BYTES = 1024 + 2 * HB + NS * STAGE + 1024;
+};
+
+template <int RP>
+__global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__ CUtensorMap tmY,
+                                                         const __grid_constant__ CUtensorMap tmB, TcExpArgs p) {
+  using C = ExpCfg<RP>;
+  constexpr int NS = C::NS, PW = C::PW, ND = C::ND;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *hbuf = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *ring = hbuf + 2 * C::HB;
+  uint64_t *full = reinterpret_cast<uint64_t *>(ring + NS * C::STAGE);
+  uint64_t *empty = full + NS;
+  uint64_t *hfull = empty + NS;    // [2]
+  uint64_t *hempty = hfull + 2;    // [2]
+  uint64_t *dfull = hempty + 2;    // [ND]
+  uint64_t *dempty = dfull + ND;   // [ND]
+  uint64_t *mdone = dempty + ND;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mdone + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t u0 = sk_begin(p.U, p.G, blockIdx.x), u1 = sk_begin(p.U, p.G, blockIdx.x + 1);
+  const int nl = p.nl;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&hfull[b], 1);
+      mbar_init(&hempty[b], 1);
+    }
+    for (int b = 0; b < ND; ++b) {
+      mbar_init(&dfull[b], 1);
+      mbar_init(&dempty[b], 4);
+    }
+    mbar_init(mdone, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmY);
+      prefetch_tmap(&tmB);
+      int64_t prev = -1;
+      int hidx = 0;
+      for (int64_t u = u0; u < u1; ++u) {
+        const int64_t rb = u / nl;
+        const int lc = (int)(u % nl);
+        if (rb != prev) {
+          const int hb = hidx & 1;
+          if (hidx >= 2 && !mbar_wait(&hempty[hb], ((hidx >> 1) & 1) ^ 1)) break;
+          mbar_arrive_expect_tx(&hfull[hb], C::HB);
+          bulk_load(hbuf + hb * C::HB, p.blob + rb * (int64_t)C::HB, C::HB, &hfull[hb]);
+          prev = rb;
+          ++hidx;
+        }
+        const int g = (int)(u - u0), s = g % NS;
+        if (g >= NS && !mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) break;
+        uint8_t *st = ring + s * C::STAGE;
+        mbar_arrive_expect_tx(&full[s], C::STAGE);
+        tma_load_2d(st, &tmY, &full[s], lc * BOXC, (int)(rb * TM));
+#pragma unroll
+        for (int pp = 0; pp < RP / PW; ++pp)
+          tma_load_2d(st + C::Y_B + pp * (BOXC * PW * 2), &tmB, &full[s], pp * PW, lc * BOXC);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = tc_idesc(TM, BOXC, false, false);
+      int64_t prev = -1;
+      int hidx = 0, hb = 0;
+      bool ok = true;
+      for (int64_t u = u0; ok && u < u1; ++u) {
+        const int64_t rb = u / nl;
+        if (rb != prev) {
+          hb = hidx & 1;
+          if (!(ok = mbar_wait(&hfull[hb], (hidx >> 1) & 1))) break;
+          prev = rb;
+          ++hidx;
+        }
+        const int g = (int)(u - u0), s = g % NS, b = g % ND;
+        if (g >= ND && !(ok = mbar_wait(&dempty[b], ((g / ND) & 1) ^ 1))) break;
+        if (!(ok = mbar_wait(&full[s], (g / NS) & 1))) break;
+        tc_fence_after();
+        const uint32_t hh = smem_u32(hbuf + hb * C::HB), bb = smem_u32(ring + s * C::STAGE) + C::Y_B;
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int qk = 0; qk < RP / 16; ++qk) {
+            const int pan = (qk * 16) / PW, in = ((qk * 16) % PW) * 2;
+            const uint64_t ad = tc_desc(hh + part * blob_tile(RP) + pan * (TM * PW * 2) + in, 16, 8 * PW * 2, PW * 2);
+            const uint64_t bd = tc_desc(bb + pan * (BOXC * PW * 2) + in, 16, 8 * PW * 2, PW * 2);
+            tc_mma_bf16(tmem + b * BOXC, ad, bd, idesc, (part == 0 && qk == 0) ? 0u : 1u);
+          }
+        tc_commit(&dfull[b]);
+        if (u == u1 - 1 || (u + 1) / nl != rb) tc_commit(&hempty[hb]);
+      }
+      tc_commit(mdone);
+      mbar_wait(mdone, 0);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3, row = 32 * q + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+    const float scale = p.scale;
+    for (int64_t u = u0; u < u1; ++u) {
+      const int g = (int)(u - u0), s = g % NS, b = g % ND;
+      if (!wait_warp(&dfull[b], (g / ND) & 1) || !wait_warp(&full[s], (g / NS) & 1)) break;
+      tc_fence_after();
+      float acc[64];
+      tmem_ld32(tl + b * BOXC, acc);
+      tmem_ld32(tl + b * BOXC + 32, acc + 32);
+      tc_fence_before();
+      const uint8_t *yt = ring + s * C::STAGE;
+      // the new row, computed before the stage is released: every read of the
+      // stage has returned its value by then, and the proxy fence orders these
+      // reads before the next TMA write of the stage
+      uint32_t o[8][4];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 yv = *reinterpret_cast<const uint4 *>(yt + swz(row, c * 16, 128));
+        const uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 y = unpack_bf16(w[e]);
+          o[c][e] = pack_bf16(y.x + scale * acc[8 * c + 2 * e], y.y + scale * acc[8 * c + 2 * e + 1]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&dempty[b]);
+        mbar_arrive(&empty[s]);
+      }
+      const int64_t rb = u / nl, grow = rb * TM + row;
+      const int l0 = (int)(u % nl) * BOXC;
+      if (grow >= p.M) continue;
+      __nv_bfloat16 *yr = p.Y + grow * p.ldy + l0;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int col = l0 + 8 * c;
+        if (col + 8 <= p.L) {
+          *reinterpret_cast<uint4 *>(yr + 8 * c) = make_uint4(o[c][0], o[c][1], o[c][2], o[c][3]);
+        } else {
+          for (int e = 0; e < 8 && col + e < p.L; ++e)
+            yr[8 * c + e] = reinterpret_cast<const __nv_bfloat16 *>(o[c])[e];
+        }
+      }
+    }
+  }
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM);
+  }
+}
+
+// ============================================================================= column pass
+template <int RP, bool kDX>
+struct ColCfg {
+  static constexpr int PW = pw_of(RP);
+  static constexpr int IN_B = 2 * TM * BOXC * 2;   // two 64-column boxes: 32 KB
+  static constexpr int BL_B = 2 * blob_tile(RP);   // hi + lo
+  static constexpr int STAGE = IN_B + BL_B;
+  static constexpr int AC_B = kDX ? 2 * RP * 128 : 0;   // A^T for dX: two [RP][64] boxes
+  static constexpr int NS0 = (kRingBytes + 28 * 1024 - AC_B) / STAGE;
+  static constexpr int NS = NS0 > 6 ? 6 : NS0;
+  static constexpr int TMEM = tmem_cols(2 * RP + (kDX ? 2 * TM : 0));
+  static constexpr int ACC0 = kDX ? 2 * TM : 0;   // first TMEM column of the accumulators
+  static constexpr int BYTES = 1024 + NS * STAGE + AC_B + 1024;
+};
+
+template <int RP, bool kDX, bool kAccX>
+__global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CUtensorMap tmIn,
+                                                      const __grid_constant__ CUtensorMap tmAc, TcColArgs p) {
+  using C = ColCfg<RP, kDX>;
+  constexpr int NS = C::NS, PW = C::PW;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *acbuf = ring + NS * C::STAGE;
+  uint64_t *full = reinterpret_cast<uint64_t *>(acbuf + C::AC_B);
+  uint64_t *empty = full + NS;
+  uint64_t *afull = empty + NS;    // [2] accumulators
+  uint64_t *aempty = afull + 2;
+  uint64_t *dfull = aempty + 2;    // [2] dX tiles
+  uint64_t *dempty = dfull + 2;
+  uint64_t *acfull = dempty + 2;   // A^T tile loaded
+  uint64_t *acempty = acfull + 1;  // A^T tile no longer read
+  uint64_t *mdone = acempty + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mdone + 1);
+  int *s_flag = reinterpret_cast<int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x;
+  const int64_t u0 = sk_begin(p.U, p.G, i), u1 = sk_begin(p.U, p.G, i + 1);
+  const int nt = p.nt;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&afull[b], 1);
+      mbar_init(&aempty[b], 4);
+      mbar_init(&dfull[b], 1);
+      mbar_init(&dempty[b], 4);
+    }
+    mbar_init(acfull, 1);
+    mbar_init(acempty, 1);
+    mbar_init(mdone, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmIn);
+      if (kDX) prefetch_tmap(&tmAc);
+      int seg = 0;
+      for (int64_t u = u0; u < u1; ++u) {
+        const int cb = (int)(u / nt), t = (int)(u % nt);
+        if (kDX && (u == u0 || t == 0)) {
+          if (seg >= 1 && !mbar_wait(acempty, (seg - 1) & 1)) break;
+          mbar_arrive_expect_tx(acfull, C::AC_B);
+          tma_load_2d(acbuf, &tmAc, acfull, cb * 2 * BOXC, 0);
+          tma_load_2d(acbuf + RP * 128, &tmAc, acfull, cb * 2 * BOXC + BOXC, 0);
+          ++seg;
+        }
+        const int g = (int)(u - u0), s = g % NS;
+        if (g >= NS && !mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) break;
+        uint8_t *st = ring + s * C::STAGE;
+        mbar_arrive_expect_tx(&full[s], C::STAGE);
+        tma_load_2d(st, &tmIn, &full[s], cb * 2 * BOXC, t * TM);
+        tma_load_2d(st + TM * BOXC * 2, &tmIn, &full[s], cb * 2 * BOXC + BOXC, t * TM);
+        bulk_load(st + C::IN_B, p.blob + (int64_t)t * C::BL_B, C::BL_B, &full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_acc = tc_idesc(TM, RP, true, true);
+      const uint32_t id_dx = tc_idesc(TM, 2 * BOXC, false, true);
+      int seg = 0;
+      bool ok = true;
+      for (int64_t u = u0; ok && u < u1; ++u) {
+        const int g = (int)(u - u0), s = g % NS;
+        const int t = (int)(u % nt);
+        const bool first = u == u0 || t == 0, last = u == u1 - 1 || t == nt - 1;
+        const int ab = seg & 1;
+        if (first) {
+          if (seg >= 2 && !(ok = mbar_wait(&aempty[ab], ((seg >> 1) & 1) ^ 1))) break;
+          if (kDX && !(ok = mbar_wait(acfull, seg & 1))) break;
+        }
+        if (!(ok = mbar_wait(&full[s], (g / NS) & 1))) break;
+        const int db = g & 1;
+        if (kDX && g >= 2 && !(ok = mbar_wait(&dempty[db], ((g >> 1) & 1) ^ 1))) break;
+        tc_fence_after();
+        const uint32_t st = smem_u32(ring + s * C::STAGE), bl = st + C::IN_B;
+        if (kDX) {
+          // dX tile [128 rows][128 columns] = (dyb_hi + dyb_lo) * A^T
+          const uint32_t ac = smem_u32(acbuf);
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int qk = 0; qk < RP / 16; ++qk) {
+              const int pan = (qk * 16) / PW, in = ((qk * 16) % PW) * 2;
+              const uint64_t ad =
+                  tc_desc(bl + part * blob_tile(RP) + pan * (TM * PW * 2) + in, 16, 8 * PW * 2, PW * 2);
+              const uint64_t bd = tc_desc(ac + qk * 2048, RP * 128, 1024, 128);
+              tc_mma_bf16(tmem + db * TM, ad, bd, id_dx, (part == 0 && qk == 0) ? 0u : 1u);
+            }
+          tc_commit(&dfull[db]);
+        }
+        // acc[c][j] += sum over the tile's 128 rows of In[row][c] * blob[row][j]
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int kk = 0; kk < TM / 16; ++kk) {
+            const uint64_t ad = tc_desc(st + kk * 2048, TM * BOXC * 2, 1024, 128);
+            const uint64_t bd =
+                tc_desc(bl + part * blob_tile(RP) + kk * 16 * PW * 2, RP > PW ? TM * PW * 2 : 16, 8 * PW * 2, PW * 2);
+            tc_mma_bf16(tmem + C::ACC0 + ab * RP, ad, bd, id_acc, (first && part == 0 && kk == 0) ? 0u : 1u);
+          }
+        tc_commit(&empty[s]);
+        if (last) {
+          tc_commit(&afull[ab]);
+          if (kDX) tc_commit(acempty);
+          ++seg;
+        }
+      }
+      tc_commit(mdone);
+      mbar_wait(mdone, 0);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3, row = 32 * q + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+    int seg = 0;
+    bool ok = true;   // after a timed-out wait: skip the work, keep the barrier sequence
+    float v[RP];
+    for (int64_t u = u0; u < u1; ++u) {
+      const int g = (int)(u - u0);
+      const int cb = (int)(u / nt), t = (int)(u % nt);
+      const bool last = u == u1 - 1 || t == nt - 1;
+      if (kDX && ok) ok = wait_warp(&dfull[g & 1], (g >> 1) & 1);
+      if (kDX && ok) {
+        const int db = g & 1;
+        tc_fence_after();
+        const int64_t grow = (int64_t)t * TM + row;
+        __nv_bfloat16 *dxr = p.dX + grow * p.lddx;
+        const float sc = p.scale;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 2 * BOXC; c0 += 32) {
+          float d[32];
+          tmem_ld32(tl + db * TM + c0, d);
+          const int col0 = cb * 2 * BOXC + c0;
+          if (grow < p.M) {
+#pragma unroll
+            for (int c8 = 0; c8 < 32; c8 += 8) {
+              const int col = col0 + c8;
+              if (col >= p.C) break;
+              float x[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] = sc * d[c8 + e];
+              if (kAccX) {
+                if (col + 8 <= p.C) {
+                  const uint4 o = *reinterpret_cast<const uint4 *>(dxr + col);
+                  const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const float2 f = unpack_bf16(w[e]);
+                    x[2 * e] += f.x;
+                    x[2 * e + 1] += f.y;
+                  }
+                } else {
+                  for (int e = 0; e < 8 && col + e < p.C; ++e) x[e] += __bfloat162float(dxr[col + e]);
+                }
+              }
+              uint32_t o[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) o[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+              if (col + 8 <= p.C) {
+                *reinterpret_cast<uint4 *>(dxr + col) = make_uint4(o[0], o[1], o[2], o[3]);
+              } else {
+                for (int e = 0; e < 8 && col + e < p.C; ++e)
+                  dxr[col + e] = reinterpret_cast<const __nv_bfloat16 *>(o)[e];
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dempty[db]);
+      }
+      if (!last) continue;
+      const int ab = seg & 1;
+      if (ok) ok = wait_warp(&afull[ab], (seg >> 1) & 1);
+#pragma unroll
+      for (int j = 0; j < RP; ++j) v[j] = 0.f;
+      if (ok) {
+        tc_fence_after();
+        tmem_row<RP>(tl + C::ACC0 + ab * RP, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&aempty[ab]);
+      }
+      ++seg;
+      if (!reduce_segment<RP>(p.U, p.G, i, cb, nt, p.part, p.counters + cb, row, v, s_flag)) continue;
+      const int64_t c = (int64_t)cb * TM + row;
+      if (c < p.C) {
+#pragma unroll
+        for (int j = 0; j < RP; ++j) {
+          if (j >= p.r) break;
+          const int64_t o = c * p.out_sc + (int64_t)j * p.out_sj;
+          if (p.out_bf16) reinterpret_cast<__nv_bfloat16 *>(p.out)[o] = __float2bfloat16_rn(p.out_scale * v[j]);
+          else reinterpret_cast<float *>(p.out)[o] = p.out_scale * v[j];
+        }
+      }
+    }
+  }
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM);
+  }
+}
+
+// ============================================================================= saved h -> blob
+// The saved h (fp32 [M][ldh], columns j < r; zero past r and past M) as a blob,
+// one 128-row block per CTA.
+template <int RP>
+__global__ void __launch_bounds__(256) hblob_kernel(const float *__restrict__ h, int64_t ldh, int64_t M, int r,
+                                                    uint8_t *blob) {
+  pdl_wait();
+  uint8_t *bhi = blob + (size_t)blockIdx.x * 2 * blob_tile(RP), *blo = bhi + blob_tile(RP);
+  const int64_t m0 = (int64_t)blockIdx.x * TM;
+  for (int e = threadIdx.x; e < TM * RP / 8; e += blockDim.x) {
+    const int row = e / (RP / 8), col = 8 * (e % (RP / 8));
+    const int64_t m = m0 + row;
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = m < M && col + k < r ? h[m * ldh + col + k] : 0.f;
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) split_bf16(v[2 * k], v[2 * k + 1], hi[k], lo[k]);
+    const uint32_t o = blob_off<RP>(row, col);
+    *reinterpret_cast<uint4 *>(bhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4 *>(blo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+  pdl_launch_dependents();
+}
+
+}  // namespace tc
+
+// ----------------------------------------------------------------------------- host side
+namespace {
+
+using namespace tc;
+
+// Big row-major bf16 operand [rows][cols] with row stride ld: boxes of 64 columns x 128 rows.
+bool map_big128(CUtensorMap *m, const void *p, int64_t rows, int64_t cols, int64_t ld) {
+  uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+  uint64_t str[1] = {(uint64_t)ld * 2};
+  uint32_t box[2] = {64, 128};
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+// Ac [r][K] (k contiguous, row stride lda): boxes of 64 k x RP rows.
+bool map_ac_tc(CUtensorMap *m, const void *p, int64_t K, int r, int64_t lda, int RP) {
+  uint64_t dims[2] = {(uint64_t)K, (uint64_t)r};
+  uint64_t str[1] = {(uint64_t)lda * 2};
+  uint32_t box[2] = {64, (uint32_t)RP};
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+// Bc [L][r] (j contiguous, row stride ldb): boxes of PW j x 64 rows.
+bool map_bc_tc(CUtensorMap *m, const void *p, int64_t L, int r, int64_t ldb, int RP) {
+  const int PW = RP < 64 ? RP : 64;
+  uint64_t dims[2] = {(uint64_t)r, (uint64_t)L};
+  uint64_t str[1] = {(uint64_t)ldb * 2};
+  uint32_t box[2] = {(uint32_t)PW, 64};
+  const CUtensorMapSwizzle sw = PW >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : PW == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : CU_TENSOR_MAP_SWIZZLE_32B;
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p, dims, str, box, sw);
+}
+
+// Persistent grid: every SM holds one CTA of these kernels (their shared memory
+// allows no more), at most one CTA per unit.
+int grid_for(int64_t units, const void *kern, size_t smem);
+
+// Stream-K passes give every CTA at least kMinUnits units (fewer CTAs on small
+// problems, and a bound on the partial sums), at most kMaxGrid CTAs (one per SM;
+// more than any GB300 has), so that workspace sizes depend on the arguments only.
+constexpr int kMinUnits = 8;
+constexpr int kMaxGrid = 160;
+int grid_for(int64_t units, const void *kern, size_t smem, int min_units) {
+  const int occ = occupancy(kern, NTHR, smem);
+  return (int)std::max<int64_t>(
+      1, std::min<int64_t>({ceil_div(units, min_units), (int64_t)occ * num_sms(), (int64_t)kMaxGrid}));
+}
+// partial-sum slots (two per CTA) of a stream-K pass over U units
+int64_t part_slots(int64_t U) { return 2 * std::max<int64_t>(1, std::min<int64_t>(ceil_div(U, kMinUnits), kMaxGrid)); }
+
+// workspace of one rows pass (partials, blob) and one column pass (partials);
+// the counters are counted by the caller
+template <int RP>
+size_t ws_rows(int64_t M, int64_t C) {
+  const int64_t nrb = ceil_div(M, TM), nc = ceil_div(C, BOXC);
+  return ws_round((size_t)part_slots(nrb * nc) * TM * RP * 4) + ws_round((size_t)nrb * 2 * blob_tile(RP));
+}
+template <int RP>
+size_t ws_col(int64_t M, int64_t C) {
+  const int64_t nt = ceil_div(M, TM), ncb = ceil_div(C, TM);
+  return ws_round((size_t)part_slots(ncb * nt) * TM * RP * 4);
+}
+
+// h = In * W (W = A: K-major, kWMN = false; W = B^T from B in PEFT layout: kWMN = true)
+// into the blob (and fp32 rows into hout when given).
+template <int RP, bool kWMN>
+lora_status_t launch_rows(const void *in, int64_t ld_in, int64_t M, int64_t Cdim, int r, const CUtensorMap &tW,
+                          int *counters, WsCarver &ws, uint8_t **blob_out, float *hout, int64_t ldh, cudaStream_t st) {
+  using Cf = RowsCfg<RP, kWMN>;
+  auto kern = rows_kernel<RP, kWMN>;
+  LORA_CUDA(ensure_smem((const void *)kern, Cf::BYTES));
+  const int64_t nrb = ceil_div(M, TM), nc = ceil_div(Cdim, BOXC);
+  const int G = grid_for(nrb * nc, (const void *)kern, Cf::BYTES, kMinUnits);
+  float *part = (float *)ws.take((size_t)2 * G * TM * RP * 4);
+  uint8_t *blob = (uint8_t *)ws.take((size_t)nrb * 2 * blob_tile(RP));
+  if (!part || !blob) return LORA_ERR_WORKSPACE;
+  CUtensorMap tIn;
+  if (!map_big128(&tIn, in, M, Cdim, ld_in)) return LORA_ERR_ALIGNMENT;
+  TcRowsArgs p{};
+  p.M = (int)M;
+  p.C = (int)Cdim;
+  p.r = r;
+  p.nc = (int)nc;
+  p.U = nrb * nc;
+  p.G = G;
+  p.part = part;
+  p.counters = counters;
+  p.blob = blob;
+  p.hout = hout;
+  p.ldh = ldh;
+  LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(NTHR), Cf::BYTES, st, 1, true, tIn, tW, p));
+  *blob_out = blob;
+  return LORA_OK;
+}
+
+// acc = In^T * blob over 128-column blocks of In (dA or dB^T), with the dX tiles when kDX.
+template <int RP, bool kDX>
+lora_status_t launch_col(const void *in, int64_t ld_in, int64_t M, int64_t Cdim, int r, const uint8_t *blob,
+                         const CUtensorMap *tAc, float scale, void *out, int64_t out_sc, int64_t out_sj, bool out_bf16,
+                         void *dX, int64_t lddx, bool dx_acc, int *counters, WsCarver &ws, cudaStream_t st) {
+  using Cf = ColCfg<RP, kDX>;
+  auto kern = kDX ? (dx_acc ? col_kernel<RP, true, true> : col_kernel<RP, true, false>) : col_kernel<RP, false, false>;
+  LORA_CUDA(ensure_smem((const void *)kern, Cf::BYTES));
+  const int64_t nt = ceil_div(M, TM), ncb = ceil_div(Cdim, TM);
+  const int G = grid_for(ncb * nt, (const void *)kern, Cf::BYTES, kMinUnits);
+  float *part = (float *)ws.take((size_t)2 * G * TM * RP * 4);
+  if (!part) return LORA_ERR_WORKSPACE;
+  CUtensorMap tIn;
+  if (!map_big128(&tIn, in, M, Cdim, ld_in)) return LORA_ERR_ALIGNMENT;
+  TcColArgs p{};
+  p.M = (int)M;
+  p.C = (int)Cdim;
+  p.r = r;
+  p.nt = (int)nt;
+  p.U = ncb * nt;
+  p.G = G;
+  p.part = part;
+  p.counters = counters;
+  p.blob = blob;
+  p.scale = scale;
+  p.out_scale = scale;
+  p.out = out;
+  p.out_sc = out_sc;
+  p.out_sj = out_sj;
+  p.out_bf16 = out_bf16 ? 1 : 0;
+  p.dX = (__nv_bfloat16 *)dX;
+  p.lddx = lddx;
+  LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(NTHR), Cf::BYTES, st, 1, true, tIn, kDX ? *tAc : tIn, p));
+  return LORA_OK;
+}
+
+template <int RP>
+lora_status_t launch_expand(const uint8_t *blob, const SingleArgs &a, const CUtensorMap &tB, cudaStream_t st) {
+  using Cf = ExpCfg<RP>;
+  auto kern = expand_kernel<RP>;
+  LORA_CUDA(ensure_smem((const void *)kern, Cf::BYTES));
+  const int64_t nrb = ceil_div(a.M, TM), nl = ceil_div(a.L, BOXC);
+  const int G = grid_for(nrb * nl, (const void *)kern, Cf::BYTES, 1);
+  CUtensorMap tY;
+  if (!map_big128(&tY, a.Y, a.M, a.L, a.ldy)) return LORA_ERR_ALIGNMENT;
+  TcExpArgs p{};
+  p.M = (int)a.M;
+  p.L = (int)a.L;
+  p.nl = (int)nl;
+  p.U = nrb * nl;
+  p.G = G;
+  p.blob = blob;
+  p.Y = (__nv_bfloat16 *)a.Y;
+  p.ldy = a.ldy;
+  p.scale = a.scale;
+  LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(NTHR), Cf::BYTES, st, 1, true, tY, tB, p));
+  return LORA_OK;
+}
+
+lora_status_t pack_tc(const SingleArgs &a, const SingleLayout &lay, WsCarver &ws, const void **Ac, const void **Bc,
+                      cudaStream_t st) {
+  if (lay.pack_A) {
+    void *d = ws.take((size_t)a.r * lay.lda * 2);
+    if (!d) return LORA_ERR_WORKSPACE;
+    LORA_TRY(pack_bf16_2d(a.A, a.sA_r, a.sA_k, a.r, a.K, d, lay.lda, st));
+    *Ac = d;
+  } else if (Ac) {
+    *Ac = a.A;
+  }
+  if (lay.pack_B) {
+    void *d = ws.take((size_t)a.L * lay.ldb * 2);
+    if (!d) return LORA_ERR_WORKSPACE;
+    LORA_TRY(pack_bf16_2d(a.B, a.sB_l, a.sB_r, a.L, a.r, d, lay.ldb, st));
+    *Bc = d;
+  } else if (Bc) {
+    *Bc = a.B;
+  }
+  return LORA_OK;
+}
+
+// Ticket counters of every stream-K pass of one op, zeroed by one memset.
+int *take_counters(WsCarver &ws, int64_t n, cudaStream_t st, lora_status_t *err) {
+  int *c = (int *)ws.take((size_t)n * 4);
+  if (!c) {
+    *err = LORA_ERR_WORKSPACE;
+    return nullptr;
+  }
+  *err = cudaMemsetAsync(c, 0, (size_t)n * 4, st) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+  return c;
+}
+
+template <int RP>
+lora_status_t forward_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st) {
+  SingleLayout lay = plan_layout(a, true, a.L > 0);
+  WsCarver carver(ws, ws_bytes);
+  const void *Ac = nullptr, *Bc = nullptr;
+  lora_status_t e;
+  int *cnt = take_counters(carver, ceil_div(a.M, TM), st, &e);
+  LORA_TRY(e);
+  LORA_TRY(pack_tc(a, lay, carver, &Ac, &Bc, st));
+  CUtensorMap tA, tB;
+  if (!map_ac_tc(&tA, Ac, a.K, a.r, lay.lda, RP)) return LORA_ERR_ALIGNMENT;
+  uint8_t *blob = nullptr;
+  LORA_TRY((launch_rows<RP, false>(a.X, a.ldx, a.M, a.K, a.r, tA, cnt, carver, &blob, a.h, a.ldh, st)));
+  if (a.L == 0) return LORA_OK;
+  if (!map_bc_tc(&tB, Bc, a.L, a.r, lay.ldb, RP)) return LORA_ERR_ALIGNMENT;
+  return launch_expand<RP>(blob, a, tB, st);
+}
+
+// dyb blob, then dX and dA; cnt holds ceil(M/128) + ceil(K/128) counters
+template <int RP>
+lora_status_t dxda_rp(const SingleArgs &a, int *cnt, WsCarver &carver, cudaStream_t st) {
+  SingleLayout lay = plan_layout(a, true, true);
+  const void *Ac = nullptr, *Bc = nullptr;
+  LORA_TRY(pack_tc(a, lay, carver, &Ac, &Bc, st));
+  CUtensorMap tA, tB;
+  if (!map_ac_tc(&tA, Ac, a.K, a.r, lay.lda, RP) || !map_bc_tc(&tB, Bc, a.L, a.r, lay.ldb, RP))
+    return LORA_ERR_ALIGNMENT;
+  uint8_t *blob = nullptr;
+  LORA_TRY((launch_rows<RP, true>(a.dY, a.lddy, a.M, a.L, a.r, tB, cnt, carver, &blob, nullptr, 0, st)));
+  return launch_col<RP, true>(a.X, a.ldx, a.M, a.K, a.r, blob, &tA, a.scale, a.dA, a.sdA_k, a.sdA_r, a.grad_lo != 0,
+                              a.dX, a.lddx, a.dx_acc != 0, cnt + ceil_div(a.M, TM), carver, st);
+}
+
+// dB from a blob of h; cnt holds ceil(L/128) counters
+template <int RP>
+lora_status_t db_from_blob(const SingleArgs &a, const uint8_t *hblob, int *cnt, WsCarver &carver, cudaStream_t st) {
+  return launch_col<RP, false>(a.dY, a.lddy, a.M, a.L, a.r, hblob, nullptr, a.scale, a.dB, a.sdB_l, a.sdB_r,
+                               a.grad_lo != 0, nullptr, 0, false, cnt, carver, st);
+}
+
+template <int RP>
+lora_status_t dxda_op(const SingleArgs &a, WsCarver &carver, cudaStream_t st) {
+  lora_status_t e;
+  int *cnt = take_counters(carver, ceil_div(a.M, TM) + ceil_div(a.K, TM), st, &e);
+  LORA_TRY(e);
+  return dxda_rp<RP>(a, cnt, carver, st);
+}
+
+template <int RP>
+lora_status_t db_op(const SingleArgs &a, WsCarver &carver, cudaStream_t st) {
+  lora_status_t e;
+  const int64_t nrb = ceil_div(a.M, TM);
+  int *cnt = take_counters(carver, nrb + ceil_div(a.L, TM), st, &e);
+  LORA_TRY(e);
+  SingleLayout lay = plan_layout(a, true, false);
+  const void *Ac = nullptr;
+  LORA_TRY(pack_tc(a, lay, carver, &Ac, nullptr, st));
+  CUtensorMap tA;
+  if (!map_ac_tc(&tA, Ac, a.K, a.r, lay.lda, RP)) return LORA_ERR_ALIGNMENT;
+  uint8_t *blob = nullptr;
+  LORA_TRY((launch_rows<RP, false>(a.X, a.ldx, a.M, a.K, a.r, tA, cnt, carver, &blob, nullptr, 0, st)));
+  return db_from_blob<RP>(a, blob, cnt + nrb, carver, st);
+}
+
+template <int RP>
+lora_status_t backward_op(const SingleArgs &a, WsCarver &carver, cudaStream_t st) {
+  lora_status_t e;
+  const int64_t nrb = ceil_div(a.M, TM), nkb = ceil_div(a.K, TM);
+  int *cnt = take_counters(carver, nrb + nkb + ceil_div(a.L, TM), st, &e);
+  LORA_TRY(e);
+  LORA_TRY(dxda_rp<RP>(a, cnt, carver, st));
+  uint8_t *hb = (uint8_t *)carver.take((size_t)nrb * 2 * blob_tile(RP));
+  if (!hb) return LORA_ERR_WORKSPACE;
+  LORA_CUDA(launch(hblob_kernel<RP>, dim3((unsigned)nrb), dim3(256), 0, st, 1, true, (const float *)a.h, a.ldh, a.M,
+                   a.r, hb));
+  return db_from_blob<RP>(a, hb, cnt + nrb + nkb, carver, st);
+}
+
+template <typename F>
+auto by_rank(int r, F f) -> decltype(f(std::integral_constant<int, 16>())) {
+  switch (rank_bucket(r)) {
+    case 16: return f(std::integral_constant<int, 16>());
+    case 32: return f(std::integral_constant<int, 32>());
+    case 64: return f(std::integral_constant<int, 64>());
+    default: return f(std::integral_constant<int, 128>());
+  }
+}
+
+}  // namespace
+
+size_t tc_ws_bytes(int op, int64_t M, int64_t K, int64_t L, int r) {
+  if (M <= 0 || K < 0 || L < 0 || r <= 0) return 0;
+  const size_t packA = ws_round((size_t)r * round_up(K, 8) * 2);
+  const size_t packB = ws_round((size_t)L * round_up(r, 8) * 2);
+  const int64_t nrb = ceil_div(M, TM), nkb = ceil_div(K, TM), nlb = ceil_div(L, TM);
+  return by_rank(r, [&](auto rp) -> size_t {
+    constexpr int RP = decltype(rp)::value;
+    const size_t hb = ws_round((size_t)nrb * 2 * blob_tile(RP));
+    if (op == LORA_OP_FORWARD) return ws_round((size_t)nrb * 4) + packA + packB + ws_rows<RP>(M, K);
+    if (op == LORA_OP_BACKWARD_DX_DA)
+      return ws_round((size_t)(nrb + nkb) * 4) + packA + packB + ws_rows<RP>(M, L) + ws_col<RP>(M, K);
+    if (op == LORA_OP_BACKWARD_DB)
+      return ws_round((size_t)(nrb + nlb) * 4) + packA + ws_rows<RP>(M, K) + ws_col<RP>(M, L);
+    if (op == LORA_OP_BACKWARD)
+      return ws_round((size_t)(nrb + nkb + nlb) * 4) + packA + packB + ws_rows<RP>(M, L) + ws_col<RP>(M, K) + hb +
+             ws_col<RP>(M, L);
+    return (size_t)0;
+  });
+}
+
+lora_status_t forward_tc(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st) {
+  return by_rank(a.r, [&](auto rp) { return forward_rp<decltype(rp)::value>(a, ws, ws_bytes, st); });
+}
+lora_status_t backward_dx_da_tc(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st) {
+  WsCarver c(ws, ws_bytes);
+  return by_rank(a.r, [&](auto rp) { return dxda_op<decltype(rp)::value>(a, c, st); });
+}
+lora_status_t backward_db_tc(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st) {
+  WsCarver c(ws, ws_bytes);
+  return by_rank(a.r, [&](auto rp) { return db_op<decltype(rp)::value>(a, c, st); });
+}
+lora_status_t backward_tc(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st) {
+  WsCarver c(ws, ws_bytes);
+  return by_rank(a.r, [&](auto rp) { return backward_op<decltype(rp)::value>(a, c, st); });
+}
+
+int read_clear_error_single_tc() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return -1;
+  if (v) cudaMemcpyToSymbol(g_device_error, &z, sizeof(int));
+  return v;
+}
+
+}  // namespace lora

@@ -1,0 +1,63 @@
+// single_tc.h -- arguments of the tensor-core (tcgen05) single-adapter kernels
+// and their host entry points.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "single_bf16.h"
+
+namespace lora {
+
+// rows_kernel: out[m, :] = In[m, :] * W for 128-row blocks, stream-K over
+// (row block, 64-column chunk) units.
+struct TcRowsArgs {
+  int M, C, r, nc;           // rows, contraction length, rank, 64-column chunks
+  int64_t U;                 // units = row blocks * nc
+  int G;                     // grid
+  float *part;               // partial sums [2 per CTA][128][RP]
+  int *counters;             // [row block], zero before the launch
+  uint8_t *blob;             // out: hi / lo bf16 tiles per row block
+  float *hout;               // out (optional): fp32 rows [M][ldh], columns < r
+  int64_t ldh;
+};
+
+// col_kernel: acc[c, :] = sum_m In[m, c] * blob[m, :] for 128-column blocks,
+// stream-K over (column block, 128-row tile) units; optionally the dX tiles.
+struct TcColArgs {
+  int M, C, r, nt;           // rows, columns of In, rank, 128-row tiles
+  int64_t U;
+  int G;
+  float *part;               // [2 per CTA][128][RP]
+  int *counters;             // [column block], zero before the launch
+  const uint8_t *blob;       // hi / lo tiles per row tile
+  float scale;               // dX = scale * blob * A^T
+  float out_scale;           // out = out_scale * acc
+  void *out;                 // out(c, j) at out[c * out_sc + j * out_sj], fp32 or bf16
+  int64_t out_sc, out_sj;
+  int out_bf16;
+  __nv_bfloat16 *dX;         // dX [M][lddx] (kDX)
+  int64_t lddx;
+};
+
+// expand_kernel: Y += scale * h * B over (row block, 64-column chunk) units.
+struct TcExpArgs {
+  int M, L, nl;
+  int64_t U;
+  int G;
+  const uint8_t *blob;       // hi / lo tiles of h per row block
+  __nv_bfloat16 *Y;
+  int64_t ldy;
+  float scale;
+};
+
+size_t tc_ws_bytes(int op, int64_t M, int64_t K, int64_t L, int r);
+lora_status_t forward_tc(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
+lora_status_t backward_dx_da_tc(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
+lora_status_t backward_db_tc(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
+lora_status_t backward_tc(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
+int read_clear_error_single_tc();
+
+}  // namespace lora
