@@ -81,6 +81,8 @@ __host__ __device__ __forceinline__ int sk_cta(int64_t U, int G, int64_t u) {
   return i;
 }
 
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
 __device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
@@ -320,6 +322,7 @@ struct ExpCfg {
 
 template <int RP>
 __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__ CUtensorMap tmY,
+                                                         const __grid_constant__ CUtensorMap tmYs,
                                                          const __grid_constant__ CUtensorMap tmB, TcExpArgs p) {
   using C = ExpCfg<RP>;
   constexpr int NS = C::NS, PW = C::PW, ND = C::ND;
@@ -424,9 +427,16 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
     }
     __syncwarp();
   } else {
+    // Each warp owns the 32 rows of its TMEM lane quarter: it adds s * acc into
+    // them in the staged Y tile and writes them back with one TMA store (rows
+    // past M and columns past L are clipped by the store).  A stage is released
+    // to the loader once the store of the next unit has been issued and this
+    // store has finished reading the stage.
     const int q = warp & 3, row = 32 * q + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
     const float scale = p.scale;
+    int pend = -1;   // stage whose store may still be reading it
+    if (lane == 0) prefetch_tmap(&tmYs);
     for (int64_t u = u0; u < u1; ++u) {
       const int g = (int)(u - u0), s = g % NS, b = g % ND;
       if (!wait_warp(&dfull[b], (g / ND) & 1) || !wait_warp(&full[s], (g / NS) & 1)) break;
@@ -435,41 +445,38 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
       tmem_ld32(tl + b * BOXC, acc);
       tmem_ld32(tl + b * BOXC + 32, acc + 32);
       tc_fence_before();
-      const uint8_t *yt = ring + s * C::STAGE;
-      // the new row, computed before the stage is released: every read of the
-      // stage has returned its value by then, and the proxy fence orders these
-      // reads before the next TMA write of the stage
-      uint32_t o[8][4];
+      uint8_t *yt = ring + s * C::STAGE;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const uint4 yv = *reinterpret_cast<const uint4 *>(yt + swz(row, c * 16, 128));
+        uint4 *yp = reinterpret_cast<uint4 *>(yt + swz(row, c * 16, 128));
+        const uint4 yv = *yp;
         const uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
+        uint32_t o[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 y = unpack_bf16(w[e]);
-          o[c][e] = pack_bf16(y.x + scale * acc[8 * c + 2 * e], y.y + scale * acc[8 * c + 2 * e + 1]);
+          o[e] = pack_bf16(y.x + scale * acc[8 * c + 2 * e], y.y + scale * acc[8 * c + 2 * e + 1]);
         }
+        *yp = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      fence_proxy_async_smem();
+      fence_proxy_async_smem();   // the TMA store reads what this warp wrote
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&dempty[b]);
-        mbar_arrive(&empty[s]);
-      }
-      const int64_t rb = u / nl, grow = rb * TM + row;
-      const int l0 = (int)(u % nl) * BOXC;
-      if (grow >= p.M) continue;
-      __nv_bfloat16 *yr = p.Y + grow * p.ldy + l0;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int col = l0 + 8 * c;
-        if (col + 8 <= p.L) {
-          *reinterpret_cast<uint4 *>(yr + 8 * c) = make_uint4(o[c][0], o[c][1], o[c][2], o[c][3]);
-        } else {
-          for (int e = 0; e < 8 && col + e < p.L; ++e)
-            yr[8 * c + e] = reinterpret_cast<const __nv_bfloat16 *>(o[c])[e];
+        const int64_t rb = u / nl;
+        tma_store_2d(&tmYs, yt + q * 32 * 128, (int)(u % nl) * BOXC, (int)(rb * TM) + 32 * q);
+        bulk_commit();
+        if (pend >= 0) {
+          bulk_wait_read1();
+          mbar_arrive(&empty[pend]);
         }
+        pend = s;
       }
+    }
+    if (lane == 0) {
+      bulk_wait_read_all();
+      if (pend >= 0) mbar_arrive(&empty[pend]);
+      bulk_wait_all();
     }
   }
   pdl_launch_dependents();
@@ -498,7 +505,8 @@ struct ColCfg {
 
 template <int RP, bool kDX, bool kAccX>
 __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CUtensorMap tmIn,
-                                                      const __grid_constant__ CUtensorMap tmAc, TcColArgs p) {
+                                                      const __grid_constant__ CUtensorMap tmAc,
+                                                      const __grid_constant__ CUtensorMap tmDX, TcColArgs p) {
   using C = ColCfg<RP, kDX>;
   constexpr int NS = C::NS, PW = C::PW;
   extern __shared__ uint8_t smem_raw[];
@@ -513,7 +521,8 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
   uint64_t *acfull = dempty + 2;   // A^T tile loaded
   uint64_t *acempty = acfull + 1;  // A^T tile no longer read
   uint64_t *mdone = acempty + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mdone + 1);
+  uint64_t *xfree = mdone + 1;     // [NS] the MMAs no longer read the stage's In tile
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfree + NS);
   int *s_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -521,9 +530,12 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
   const int64_t u0 = sk_begin(p.U, p.G, i), u1 = sk_begin(p.U, p.G, i + 1);
   const int nt = p.nt;
   if (threadIdx.x == 0) {
+    // with dX, a stage is released by the four epilogue warps once the dX tile
+    // they wrote over its In tile has been stored; else by the MMAs' completion
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kDX ? 4 : 1);
+      mbar_init(&xfree[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&afull[b], 1);
@@ -546,7 +558,10 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
   if (warp == 0) {
     if (lane == 0) {
       prefetch_tmap(&tmIn);
-      if (kDX) prefetch_tmap(&tmAc);
+      if (kDX) {
+        prefetch_tmap(&tmAc);
+        prefetch_tmap(&tmDX);
+      }
       int seg = 0;
       for (int64_t u = u0; u < u1; ++u) {
         const int cb = (int)(u / nt), t = (int)(u % nt);
@@ -611,7 +626,7 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
                 tc_desc(bl + part * blob_tile(RP) + kk * 16 * PW * 2, RP > PW ? TM * PW * 2 : 16, 8 * PW * 2, PW * 2);
             tc_mma_bf16(tmem + C::ACC0 + ab * RP, ad, bd, id_acc, (first && part == 0 && kk == 0) ? 0u : 1u);
           }
-        tc_commit(&empty[s]);
+        tc_commit(kDX ? &xfree[s] : &empty[s]);
         if (last) {
           tc_commit(&afull[ab]);
           if (kDX) tc_commit(acempty);
@@ -627,60 +642,70 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
     int seg = 0;
     bool ok = true;   // after a timed-out wait: skip the work, keep the barrier sequence
+    int pend = -1;    // stage whose dX store may still be reading it
     float v[RP];
     for (int64_t u = u0; u < u1; ++u) {
       const int g = (int)(u - u0);
       const int cb = (int)(u / nt), t = (int)(u % nt);
       const bool last = u == u1 - 1 || t == nt - 1;
       if (kDX && ok) ok = wait_warp(&dfull[g & 1], (g >> 1) & 1);
+      if (kDX && ok) ok = wait_warp(&xfree[g % NS], (g / NS) & 1);
       if (kDX && ok) {
-        const int db = g & 1;
+        // the dX tile: scaled (and added to the old dX), rounded to bf16 and
+        // written over the stage's In tile (same swizzled layout), then each
+        // warp stores its 32 rows with TMA (rows past M and columns past K are
+        // clipped by the store)
+        const int db = g & 1, s = g % NS;
+        uint8_t *st = ring + s * C::STAGE;
         tc_fence_after();
         const int64_t grow = (int64_t)t * TM + row;
-        __nv_bfloat16 *dxr = p.dX + grow * p.lddx;
+        const __nv_bfloat16 *dxr = p.dX + grow * p.lddx;
         const float sc = p.scale;
 #pragma unroll 1
         for (int c0 = 0; c0 < 2 * BOXC; c0 += 32) {
           float d[32];
           tmem_ld32(tl + db * TM + c0, d);
-          const int col0 = cb * 2 * BOXC + c0;
-          if (grow < p.M) {
 #pragma unroll
-            for (int c8 = 0; c8 < 32; c8 += 8) {
-              const int col = col0 + c8;
-              if (col >= p.C) break;
-              float x[8];
+          for (int c8 = 0; c8 < 32; c8 += 8) {
+            const int cc = c0 + c8, col = cb * 2 * BOXC + cc;
+            float x[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) x[e] = sc * d[c8 + e];
-              if (kAccX) {
-                if (col + 8 <= p.C) {
-                  const uint4 o = *reinterpret_cast<const uint4 *>(dxr + col);
-                  const uint32_t w[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    const float2 f = unpack_bf16(w[e]);
-                    x[2 * e] += f.x;
-                    x[2 * e + 1] += f.y;
-                  }
-                } else {
-                  for (int e = 0; e < 8 && col + e < p.C; ++e) x[e] += __bfloat162float(dxr[col + e]);
-                }
-              }
-              uint32_t o[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) o[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+            for (int e = 0; e < 8; ++e) x[e] = sc * d[c8 + e];
+            if (kAccX && grow < p.M && col < p.C) {
               if (col + 8 <= p.C) {
-                *reinterpret_cast<uint4 *>(dxr + col) = make_uint4(o[0], o[1], o[2], o[3]);
+                const uint4 o = *reinterpret_cast<const uint4 *>(dxr + col);
+                const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 f = unpack_bf16(w[e]);
+                  x[2 * e] += f.x;
+                  x[2 * e + 1] += f.y;
+                }
               } else {
-                for (int e = 0; e < 8 && col + e < p.C; ++e)
-                  dxr[col + e] = reinterpret_cast<const __nv_bfloat16 *>(o)[e];
+                for (int e = 0; e < 8 && col + e < p.C; ++e) x[e] += __bfloat162float(dxr[col + e]);
               }
             }
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+            *reinterpret_cast<uint4 *>(st + (cc / BOXC) * (TM * BOXC * 2) + swz(row, (cc % BOXC) * 2, 128)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
         tc_fence_before();
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&dempty[db]);
+        if (lane == 0) {
+          mbar_arrive(&dempty[db]);
+          tma_store_2d(&tmDX, st + q * 32 * 128, cb * 2 * BOXC, t * TM + 32 * q);
+          tma_store_2d(&tmDX, st + TM * BOXC * 2 + q * 32 * 128, cb * 2 * BOXC + BOXC, t * TM + 32 * q);
+          bulk_commit();
+          if (pend >= 0) {
+            bulk_wait_read1();
+            mbar_arrive(&empty[pend]);
+          }
+          pend = s;
+        }
       }
       if (!last) continue;
       const int ab = seg & 1;
@@ -706,6 +731,11 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
           else reinterpret_cast<float *>(p.out)[o] = p.out_scale * v[j];
         }
       }
+    }
+    if (kDX && lane == 0) {
+      bulk_wait_read_all();
+      if (pend >= 0) mbar_arrive(&empty[pend]);
+      bulk_wait_all();
     }
   }
   pdl_launch_dependents();
@@ -749,12 +779,15 @@ namespace {
 
 using namespace tc;
 
-// Big row-major bf16 operand [rows][cols] with row stride ld: boxes of 64 columns x 128 rows.
-bool map_big128(CUtensorMap *m, const void *p, int64_t rows, int64_t cols, int64_t ld) {
+// Big row-major bf16 operand [rows][cols] with row stride ld: boxes of 64 columns x box_rows rows.
+bool map_rows_box(CUtensorMap *m, const void *p, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows) {
   uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
   uint64_t str[1] = {(uint64_t)ld * 2};
-  uint32_t box[2] = {64, 128};
+  uint32_t box[2] = {64, box_rows};
   return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+bool map_big128(CUtensorMap *m, const void *p, int64_t rows, int64_t cols, int64_t ld) {
+  return map_rows_box(m, p, rows, cols, ld, 128);
 }
 // Ac [r][K] (k contiguous, row stride lda): boxes of 64 k x RP rows.
 bool map_ac_tc(CUtensorMap *m, const void *p, int64_t K, int r, int64_t lda, int RP) {
@@ -849,8 +882,9 @@ lora_status_t launch_col(const void *in, int64_t ld_in, int64_t M, int64_t Cdim,
   const int G = grid_for(ncb * nt, (const void *)kern, Cf::BYTES, kMinUnits);
   float *part = (float *)ws.take((size_t)2 * G * TM * RP * 4);
   if (!part) return LORA_ERR_WORKSPACE;
-  CUtensorMap tIn;
+  CUtensorMap tIn, tDX;
   if (!map_big128(&tIn, in, M, Cdim, ld_in)) return LORA_ERR_ALIGNMENT;
+  if (kDX && !map_rows_box(&tDX, dX, M, Cdim, lddx, 32)) return LORA_ERR_ALIGNMENT;
   TcColArgs p{};
   p.M = (int)M;
   p.C = (int)Cdim;
@@ -869,7 +903,8 @@ lora_status_t launch_col(const void *in, int64_t ld_in, int64_t M, int64_t Cdim,
   p.out_bf16 = out_bf16 ? 1 : 0;
   p.dX = (__nv_bfloat16 *)dX;
   p.lddx = lddx;
-  LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(NTHR), Cf::BYTES, st, 1, true, tIn, kDX ? *tAc : tIn, p));
+  LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(NTHR), Cf::BYTES, st, 1, true, tIn, kDX ? *tAc : tIn, kDX ? tDX : tIn,
+                   p));
   return LORA_OK;
 }
 
@@ -880,8 +915,9 @@ lora_status_t launch_expand(const uint8_t *blob, const SingleArgs &a, const CUte
   LORA_CUDA(ensure_smem((const void *)kern, Cf::BYTES));
   const int64_t nrb = ceil_div(a.M, TM), nl = ceil_div(a.L, BOXC);
   const int G = grid_for(nrb * nl, (const void *)kern, Cf::BYTES, 1);
-  CUtensorMap tY;
-  if (!map_big128(&tY, a.Y, a.M, a.L, a.ldy)) return LORA_ERR_ALIGNMENT;
+  CUtensorMap tY, tYs;
+  if (!map_big128(&tY, a.Y, a.M, a.L, a.ldy) || !map_rows_box(&tYs, a.Y, a.M, a.L, a.ldy, 32))
+    return LORA_ERR_ALIGNMENT;
   TcExpArgs p{};
   p.M = (int)a.M;
   p.L = (int)a.L;
@@ -892,7 +928,7 @@ lora_status_t launch_expand(const uint8_t *blob, const SingleArgs &a, const CUte
   p.Y = (__nv_bfloat16 *)a.Y;
   p.ldy = a.ldy;
   p.scale = a.scale;
-  LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(NTHR), Cf::BYTES, st, 1, true, tY, tB, p));
+  LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(NTHR), Cf::BYTES, st, 1, true, tY, tYs, tB, p));
   return LORA_OK;
 }
 
