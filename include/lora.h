@@ -103,7 +103,9 @@ typedef struct {
 /* Bytes of workspace that `op` needs for the given sizes (an upper bound that
  * depends only on its arguments, never on device state).
  *   single-adapter ops: (dtype, M, K, L, r, 0)
- *   multi-adapter ops:  (LORA_BF16, T, in, O, R, S)   O = sum of out_slices
+ *   multi-adapter ops:  (LORA_BF16, T, in, O, R, S)   O = sum of out_slices;
+ *                       for LORA_OP_SHRINK, O = num_slices * R (the width of h),
+ *                       or 0 for a bound that holds for any num_slices
  * Returns 0 when the op needs none. */
 LORA_API size_t lora_workspace_size(lora_op_t op, lora_dtype_t dtype, int64_t m_or_t, int64_t k_or_in,
                            int64_t l_or_o, int32_t r_or_R, int32_t num_slots);

@@ -251,7 +251,7 @@ def lora_shrink(x, a, slots, ranks, R, h, num_slices=1, ws=None, stream=None):
     assert a.dim() == 3 and a.shape[0] == S and a.shape[1] == num_slices * R and a.shape[2] == IN
     assert a.stride(2) == 1
     if ws is None:
-        ws = workspace(OP_SHRINK, LORA_BF16, T, IN, 0, R, S, device=x.device)
+        ws = workspace(OP_SHRINK, LORA_BF16, T, IN, num_slices * R, R, S, device=x.device)
     ad = _addr(slots, S, R)
     st = lib().lora_shrink(ctypes.byref(ad), _ptr(ranks), IN, num_slices, _ptr(x), x.stride(0), _ptr(a),
                            a.stride(0), a.stride(1), _ptr(h), h.stride(0), *_ws_args(ws), _stream(stream))

@@ -14,6 +14,7 @@
 #include "multi.h"
 #include "single_bf16.h"
 #include "single_tc.h"
+#include "multi_tc.h"
 
 namespace lora {
 
@@ -367,7 +368,7 @@ lora_status_t lora_shrink(const lora_addressing_t *addr, const int32_t *ranks, i
   LORA_TRY(check_big(h, T, NR, ldh, 4));
   if (T > 0 && in > 0 && a == nullptr) return LORA_ERR_INVALID_ARG;
   if (in > 0 && ((sa_row * 2) % 16 != 0 || (sa_slot * 2) % 16 != 0 || !aligned16(a))) return LORA_ERR_ALIGNMENT;
-  LORA_TRY(check_ws(ws, ws_bytes, multi_ws_bytes(LORA_OP_SHRINK, T, in, 0, addr->max_rank, addr->num_slots)));
+  LORA_TRY(check_ws(ws, ws_bytes, multi_ws_bytes(LORA_OP_SHRINK, T, in, NR, addr->max_rank, addr->num_slots)));
   if (T == 0) return LORA_OK;
   MultiArgs m{};
   m.addr = *addr; m.ranks = ranks; m.in = in; m.n = num_slices; m.x = x; m.ldx = ldx; m.a = a;
@@ -439,8 +440,8 @@ lora_status_t lora_gather_shrink(const lora_addressing_t *addr, const int32_t *r
 lora_status_t lora_device_error(int32_t *code) {
   if (code == nullptr) return LORA_ERR_INVALID_ARG;
   int v = 0;
-  int parts[4] = {read_clear_error_single_bf16(), read_clear_error_single_f32(), read_clear_error_multi(),
-                  read_clear_error_single_tc()};
+  int parts[5] = {read_clear_error_single_bf16(), read_clear_error_single_f32(), read_clear_error_multi(),
+                  read_clear_error_single_tc(), read_clear_error_multi_tc()};
   for (int p : parts) {
     if (p < 0) return LORA_ERR_CUDA;
     v |= p;

@@ -28,6 +28,7 @@
 #include "common.cuh"
 #include "host_common.h"
 #include "multi.h"
+#include "multi_tc.h"
 
 namespace lora {
 
@@ -191,7 +192,7 @@ constexpr int GU = 8;   // tokens per lane per batch in group_kernel
 __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__ slots, int T, int S, int R,
                                                      const int32_t *__restrict__ ranks, int32_t *counts_out,
                                                      int32_t *perm_out, int32_t *num_active_out, int *header,
-                                                     int4 *tiles, int bmt) {
+                                                     int4 *tiles, int bmt, int *zero, int nzero) {
   extern __shared__ int gsm[];
   const int nw = blockDim.x >> 5;
   int *hist = gsm;                 // [nw][S]
@@ -201,6 +202,8 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
   int *sh = sbase + S;             // scan scratch (160 ints)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
+  // the tickets of the kernel that follows start at zero
+  for (int k = threadIdx.x; k < nzero; k += blockDim.x) zero[k] = 0;
   const int t_lo = (int)((int64_t)T * warp / nw), t_hi = (int)((int64_t)T * (warp + 1) / nw);
   const bool one_batch = t_hi - t_lo <= 32 * GU;   // the warp's slots stay in registers for both passes
   int sv[GU];
@@ -804,6 +807,73 @@ __global__ void __launch_bounds__(ExCfg<RP>::THREADS, RP >= 128 ? 2 : 3)
 }
 
 // =============================================================================
+// expand_decode_kernel: the expand for tiles of a few tokens (decode batches,
+// where every token may carry its own adapter).  The work is streaming the
+// slots' b rows; a block takes one tile and 256 output columns of one slice,
+// each thread one output column c: it loads b[slot][c][0 .. rank) once (16-byte
+// loads) and for each token t of the tile adds scal * sum_j h[t][i R + j] b[c][j]
+// into y[t][c] (the warp's 32 columns of a token row are one coalesced access).
+// Columns j >= rank of h and b are never read.
+// =============================================================================
+constexpr int DX_COLS = 256;   // output columns per block
+
+template <int RP>
+__global__ void __launch_bounds__(DX_COLS) expand_decode_kernel(MArgs p) {
+  extern __shared__ float hs[];   // [len][RP] of the tile's h rows (slice i)
+  pdl_wait();
+  const int nblk = p.ngroups;     // blocks per tile (over all slices)
+  const int tile = blockIdx.x / nblk, bi = blockIdx.x % nblk;
+  if (tile >= p.header[1]) return;
+  // block -> slice i and its first column
+  int i = 0, left = bi;
+  for (; i < p.n; ++i) {
+    const int nb = (p.off[i + 1] - p.off[i] + DX_COLS - 1) / DX_COLS;
+    if (left < nb) break;
+    left -= nb;
+  }
+  if (i >= p.n) return;
+  const int4 td = p.tiles[tile];
+  const int slot = td.x, start = td.y, len = td.z;
+  const int rank = p.ranks[slot];
+  const float sc = p.scal[slot];
+  for (int e = threadIdx.x; e < len * RP; e += blockDim.x) {
+    const int t = e / RP, j = e % RP;
+    hs[e] = j < rank ? p.h[(int64_t)p.perm[start + t] * p.ldh + (int64_t)i * p.R + j] : 0.f;
+  }
+  __syncthreads();
+  const int c = p.off[i] + left * DX_COLS + threadIdx.x;
+  if (c >= p.off[i + 1]) return;
+  // b[slot][c][0 .. rank): rank16 / 8 sixteen-byte loads, the padding masked
+  const __nv_bfloat16 *br = p.b + (int64_t)slot * p.sb_slot + (int64_t)c * p.sb_row;
+  float bv[RP];
+#pragma unroll
+  for (int j = 0; j < RP; j += 8) {
+    if (j < rank) {
+      const uint4 w = *reinterpret_cast<const uint4 *>(br + j);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_bf16(ww[e]);
+        bv[j + 2 * e] = j + 2 * e < rank ? f.x : 0.f;
+        bv[j + 2 * e + 1] = j + 2 * e + 1 < rank ? f.y : 0.f;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) bv[j + e] = 0.f;
+    }
+  }
+  for (int t = 0; t < len; ++t) {
+    const float *ht = hs + t * RP;
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < RP; ++j) acc += ht[j] * bv[j];
+    __nv_bfloat16 *yp = p.y + (int64_t)p.perm[start + t] * p.ldy + c;
+    *yp = __float2bfloat16_rn(__bfloat162float(*yp) + sc * acc);
+  }
+  pdl_launch_dependents();
+}
+
+// =============================================================================
 // gather_shrink: one warp per token; h[t, j] = a[slot][j][id] for j < rank
 // (zeros when id is outside [0, V)); an exact copy widened to fp32.
 // =============================================================================
@@ -869,7 +939,8 @@ bool carve_sched(WsCarver &c, int64_t T, int S, SchedPtrs &sp) {
 }
 
 lora_status_t launch_group(const lora_addressing_t &ad, const int32_t *ranks, int32_t *counts, int32_t *perm,
-                           int32_t *num_active, int *header, int4 *tiles, cudaStream_t st) {
+                           int32_t *num_active, int *header, int4 *tiles, cudaStream_t st, int *zero = nullptr,
+                           int nzero = 0) {
   const int S = ad.num_slots;
   int nw = (int)std::max<int64_t>(1, (160 * 1024 / 4 - 256 - 3 * S) / S);   // shared-memory bound
   // enough warps for the tokens, and for the per-slot scans (a warp scans the
@@ -879,7 +950,7 @@ lora_status_t launch_group(const lora_addressing_t &ad, const int32_t *ranks, in
   const size_t smem = (size_t)(nw * S + 3 * S + 160) * 4;
   LORA_CUDA(ensure_smem((const void *)group_kernel, smem));
   LORA_CUDA(launch(group_kernel, dim3(1), dim3(nw * 32), smem, st, 1, true, ad.slots, ad.num_tokens, S,
-                   ad.max_rank, ranks, counts, perm, num_active, header, tiles, (int)TC_M));
+                   ad.max_rank, ranks, counts, perm, num_active, header, tiles, (int)TC_M, zero, nzero));
   return LORA_OK;
 }
 
@@ -988,7 +1059,32 @@ lora_status_t launch_expand(MArgs a, int64_t T, cudaStream_t st) {
   return LORA_OK;
 }
 
+template <int RP>
+lora_status_t launch_expand_decode(MArgs a, int64_t T, cudaStream_t st) {
+  int nblk = 0;
+  for (int i = 0; i < a.n; ++i) nblk += (int)ceil_div(a.off[i + 1] - a.off[i], DX_COLS);
+  if (nblk == 0) return LORA_OK;
+  a.ngroups = nblk;
+  const int64_t tiles = max_tiles(T, a.S);
+  const size_t smem = (size_t)TC_M * RP * 4;   // h rows of the largest tile
+  LORA_CUDA(ensure_smem((const void *)expand_decode_kernel<RP>, smem));
+  LORA_CUDA(launch(expand_decode_kernel<RP>, dim3((unsigned)(tiles * nblk)), dim3(DX_COLS), smem, st, 1, true, a));
+  return LORA_OK;
+}
+
+// Decode batches (a few tokens per slot on average) stream the b rows on the
+// CUDA cores; prefill batches run the tiled expand.
+bool decode_shape(int64_t T, int S) { return T <= 4 * (int64_t)S; }
+
 lora_status_t dispatch_expand(const MArgs &a, int64_t T, cudaStream_t st) {
+  if (decode_shape(T, a.S)) {
+    switch (rank_bucket(a.R)) {
+      case 16: return launch_expand_decode<16>(a, T, st);
+      case 32: return launch_expand_decode<32>(a, T, st);
+      case 64: return launch_expand_decode<64>(a, T, st);
+      default: return launch_expand_decode<128>(a, T, st);
+    }
+  }
   switch (rank_bucket(a.R)) {
     case 16: return launch_expand<16>(a, T, st);
     case 32: return launch_expand<32>(a, T, st);
@@ -1060,15 +1156,74 @@ lora_status_t schedule_and_shrink(const MultiArgs &m, WsCarver &c, SchedPtrs &sp
   return launch_shrink(a, m.addr.num_tokens, st);
 }
 
+// Tickets of the stream-K shrink (one per tile).
+size_t tc_counter_bytes(int64_t T, int S) { return ws_round((size_t)(max_tiles(T, S) + 1) * 4); }
+// Width of the shrink output h for the workspace bound (n * R when known).
+int shrink_cols(int64_t n_times_R, int R) {
+  return (int)std::min<int64_t>(256, n_times_R > 0 ? n_times_R : (int64_t)LORA_MAX_SLICES * R);
+}
+
+MtArgs mt_args(const MultiArgs &m, const SchedPtrs &sp) {
+  MtArgs a{};
+  a.ranks = m.ranks;
+  a.scal = m.scalings;
+  a.header = sp.header;
+  a.tiles = sp.tiles;
+  a.perm = sp.perm;
+  a.S = m.addr.num_slots;
+  a.R = m.addr.max_rank;
+  a.n = m.n;
+  a.T = m.addr.num_tokens;
+  a.in = (int)m.in;
+  a.nk = (int)std::max<int64_t>(1, ceil_div(m.in, 64));
+  a.ncm = m.n * std::max(16, (int)round_up(m.addr.max_rank, 16));
+  a.h = m.h;
+  a.ldh = m.ldh;
+  return a;
+}
+
+// Schedule (grouping kernel, which also zeroes the tickets), carving the counters.
+lora_status_t tc_schedule(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, MtArgs &a, cudaStream_t st) {
+  if (!carve_sched(c, m.addr.num_tokens, m.addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
+  const int nc = max_tiles(m.addr.num_tokens, m.addr.num_slots) + 1;
+  int *cnt = (int *)c.take((size_t)nc * 4);
+  if (!cnt) return LORA_ERR_WORKSPACE;
+  LORA_TRY(launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st, cnt, nc));
+  a = mt_args(m, sp);
+  a.counters = cnt;
+  return LORA_OK;
+}
+
+// The schedule, then the shrink that suits the batch's shape: decode batches (a
+// few tokens per slot) split (tile, chunk) units evenly over a persistent grid;
+// prefill batches give each 128-token tile a cluster of CTAs.
+lora_status_t schedule_then_shrink(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, cudaStream_t st) {
+  if (!decode_shape(m.addr.num_tokens, m.addr.num_slots)) {
+    MArgs a;
+    return schedule_and_shrink(m, c, sp, &a, m.h, m.ldh, st);
+  }
+  MtArgs a;
+  LORA_TRY(tc_schedule(m, c, sp, a, st));
+  a.part = (float *)c.take(multi_tc_part_bytes(m.n, m.addr.max_rank));
+  if (!a.part) return LORA_ERR_WORKSPACE;
+  return shrink_tc_launch(a, m, m.addr.num_tokens, st);
+}
+
 }  // namespace
 
 size_t multi_ws_bytes(int op, int64_t T, int64_t in, int64_t O, int R, int S) {
   (void)in;
-  (void)O;
   if (T <= 0) return 0;
-  if (op == LORA_OP_GROUP_BY_SLOT || op == LORA_OP_EXPAND) return sched_bytes(T, S);
-  if (op == LORA_OP_SHRINK) return sched_bytes(T, S);
-  if (op == LORA_OP_APPLY_LINEAR) return sched_bytes(T, S) + hbuf_bytes(T, R);
+  if (op == LORA_OP_GROUP_BY_SLOT) return sched_bytes(T, S);
+  if (op == LORA_OP_EXPAND) return sched_bytes(T, S) + tc_counter_bytes(T, S);
+  // shrink: O carries the width of h (num_slices * R), 0 when unknown
+  if (op == LORA_OP_SHRINK) {
+    const int nc = shrink_cols(O, R);
+    return sched_bytes(T, S) + tc_counter_bytes(T, S) + ws_round(multi_tc_part_bytes(1, nc));
+  }
+  if (op == LORA_OP_APPLY_LINEAR)
+    return sched_bytes(T, S) + tc_counter_bytes(T, S) + ws_round(multi_tc_part_bytes(1, shrink_cols(0, R))) +
+           hbuf_bytes(T, R);
   return 0;
 }
 
@@ -1088,10 +1243,15 @@ lora_status_t group_by_slot(const lora_addressing_t &addr, const int32_t *ranks,
 
 lora_status_t shrink(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t st) {
   LORA_TRY(check_seg(m, true, false));
+  if (m.in == 0) {
+    // h = x * a = 0: every entry the page specifies is zero (the others may be anything)
+    LORA_CUDA(cudaMemset2DAsync(m.h, (size_t)m.ldh * 4, 0, (size_t)m.n * m.addr.max_rank * 4,
+                                (size_t)m.addr.num_tokens, st));
+    return LORA_OK;
+  }
   WsCarver c(ws, ws_bytes);
   SchedPtrs sp;
-  MArgs a;
-  return schedule_and_shrink(m, c, sp, &a, m.h, m.ldh, st);
+  return schedule_then_shrink(m, c, sp, st);
 }
 
 lora_status_t expand(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t st) {
@@ -1108,9 +1268,10 @@ lora_status_t apply_linear(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t 
   float *h = (float *)c.take(hbuf_bytes(m.addr.num_tokens, m.addr.max_rank));
   if (!h) return LORA_ERR_WORKSPACE;
   SchedPtrs sp;
-  MArgs a;
-  LORA_TRY(schedule_and_shrink(m, c, sp, &a, h, (int64_t)m.n * m.addr.max_rank, st));
-  return dispatch_expand(a, m.addr.num_tokens, st);
+  m.h = h;
+  m.ldh = (int64_t)m.n * m.addr.max_rank;
+  LORA_TRY(schedule_then_shrink(m, c, sp, st));
+  return dispatch_expand(margs(m, sp), m.addr.num_tokens, st);
 }
 
 lora_status_t gather_shrink(MultiArgs m, cudaStream_t st) {

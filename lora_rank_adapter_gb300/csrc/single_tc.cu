@@ -45,6 +45,7 @@
 #include "host_common.h"
 #include "single_bf16.h"
 #include "single_tc.h"
+#include "tc_common.cuh"
 
 namespace lora {
 namespace tc {
@@ -70,28 +71,12 @@ __device__ __forceinline__ uint32_t blob_off(int row, int col) {
   return (uint32_t)((col / PW) * (TM * PW * 2)) + swz((uint32_t)row, (uint32_t)(col % PW) * 2, PW * 2);
 }
 
-// ----------------------------------------------------------------------------- stream-K split
-// Units [0, U) are dealt to G CTAs in contiguous runs: CTA i takes [b(i), b(i+1)).
-__host__ __device__ __forceinline__ int64_t sk_begin(int64_t U, int G, int i) { return U * i / G; }
-// The CTA whose run holds unit u.
-__host__ __device__ __forceinline__ int sk_cta(int64_t U, int G, int64_t u) {
-  int i = (int)(u * G / U);
-  while (i + 1 < G && sk_begin(U, G, i + 1) <= u) ++i;
-  while (i > 0 && sk_begin(U, G, i) > u) --i;
-  return i;
-}
-
-__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-
-__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
-}
-
+// Partial sums are stored column-major ([RP columns][128 rows]): a warp's
+// accesses of one column are 32 consecutive floats.
 template <int RP>
 __device__ __forceinline__ void store_partial(float *part, int row, const float *v) {
-  float4 *p = reinterpret_cast<float4 *>(part + (int64_t)row * RP);
 #pragma unroll
-  for (int j = 0; j < RP / 4; ++j) __stcg(p + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+  for (int j = 0; j < RP; ++j) __stcg(part + j * TM + row, v[j]);
 }
 // RP accumulator columns of this thread's TMEM lane.
 template <int RP>
@@ -105,12 +90,6 @@ __device__ __forceinline__ void tmem_row(uint32_t taddr, float *v) {
 #pragma unroll
     for (int c = 0; c < RP; c += 32) tmem_ld32(taddr + c, v + c);
   }
-}
-
-// Partial sums live per CTA: a CTA's run meets a group that it does not cover
-// whole only as its first group (slot 0) or its last group (slot 1).
-__host__ __device__ __forceinline__ int64_t part_slot(int64_t U, int G, int c, int64_t g, int64_t n) {
-  return 2 * (int64_t)c + (sk_begin(U, G, c) / n == g ? 0 : 1);
 }
 
 // The epilogue's end of the segment of group g (units [g n, (g + 1) n)) that CTA
@@ -134,15 +113,9 @@ __device__ __forceinline__ bool reduce_segment(int64_t U, int G, int i, int64_t 
 #pragma unroll
     for (int j = 0; j < RP; ++j) v[j] = 0.f;
     for (int c = first; c <= last_cta; ++c) {
-      const float4 *p4 = reinterpret_cast<const float4 *>(part + (part_slot(U, G, c, g, n) * TM + row) * RP);
+      const float *pc = part + part_slot(U, G, c, g, n) * TM * RP + row;
 #pragma unroll
-      for (int j = 0; j < RP / 4; ++j) {
-        const float4 t = __ldcg(p4 + j);
-        v[4 * j] += t.x;
-        v[4 * j + 1] += t.y;
-        v[4 * j + 2] += t.z;
-        v[4 * j + 3] += t.w;
-      }
+      for (int j = 0; j < RP; ++j) v[j] += __ldcg(pc + j * TM);
     }
     if (threadIdx.x == EPI0 * 32) *counter = 0;   // ready for the next call
   }

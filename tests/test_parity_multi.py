@@ -103,6 +103,11 @@ CASES = [  # T, IN, out_slices, S, R, rank choices, layout
     (257, 96, [64, 64], 5, 64, [0, 16, 64], "segments"),
     (200, 64, [72], 3, 128, [0, 40, 128], "uniform"),
     (90, 136, [64], 4, 24, [0, 8, 24], "uniform"),
+    # decode-shaped batches (at most four tokens per slot on average)
+    (64, 256, [128, 64], 32, 64, [8, 16, 32, 64], "uniform"),
+    (200, 520, [136], 64, 32, [0, 8, 16, 24, 32], "uniform"),
+    (100, 72, [24, 40], 40, 16, [0, 8, 16], "uniform"),
+    (9, 1000, [256], 9, 128, [0, 40, 128], "uniform"),
 ]
 
 
