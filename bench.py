@@ -248,28 +248,36 @@ def make_multi_set(torch, synth, binding, dev, name, seed):
     return w
 
 
-def multi_fns(lora, binding):
+def multi_fns(lora, binding, sched=False):
+    """The segmented ops; with sched=True they reuse the batch's prebuilt schedule
+    (m["sched"], from lora_build_schedule) instead of grouping the tokens again."""
+    def sc(m):
+        return m["sched"] if sched else None
+
     def group(m):
         lora.lora_group_by_slot(m["slots"], m["ranks"], m["R"], m["counts"], m["perm"], m["nact"],
                                 ws=m["ws"][binding.OP_GROUP_BY_SLOT])
 
+    def build(m):
+        m["sched"] = lora.lora_build_schedule(m["slots"], m["ranks"], m["R"])
+
     def shrink(m):
         lora.lora_shrink(m["x"], m["a"], m["slots"], m["ranks"], m["R"], m["h"], num_slices=len(m["out_slices"]),
-                         ws=m["ws"][binding.OP_SHRINK])
+                         ws=m["ws"][binding.OP_SHRINK], schedule=sc(m))
 
     def expand(m):
         lora.lora_expand(m["h"], m["b"], m["slots"], m["ranks"], m["scalings"], m["y"], m["out_slices"], m["R"],
-                         ws=m["ws"][binding.OP_EXPAND])
+                         ws=m["ws"][binding.OP_EXPAND], schedule=sc(m))
 
     def apply(m):
         lora.lora_apply_linear(m["x"], m["a"], m["b"], m["slots"], m["ranks"], m["scalings"], m["y"],
-                               m["out_slices"], m["R"], ws=m["ws"][binding.OP_APPLY_LINEAR])
+                               m["out_slices"], m["R"], ws=m["ws"][binding.OP_APPLY_LINEAR], schedule=sc(m))
 
     def gather(m):
         lora.lora_gather_shrink(m["ids"], m["ga"], m["slots"], m["ranks"], m["R"], m["hg"])
 
-    return {"lora_group_by_slot": group, "lora_shrink": shrink, "lora_expand": expand,
-            "lora_apply_linear": apply, "lora_gather_shrink": gather}
+    return {"lora_group_by_slot": group, "lora_build_schedule": build, "lora_shrink": shrink,
+            "lora_expand": expand, "lora_apply_linear": apply, "lora_gather_shrink": gather}
 
 
 def c3_step_ops(sets, lora, binding):
@@ -424,7 +432,7 @@ def run_parts(torch, lora, binding, synth, dev, stream, c3_sets, args, peak, pea
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush = lambda: flush_buf.zero_()
     reps = args.part_reps
-    SF, MF = single_fns(lora, binding), multi_fns(lora, binding)
+    SF, MF, MS = single_fns(lora, binding), multi_fns(lora, binding), multi_fns(lora, binding, sched=True)
     out = {}
 
     def add(cfg, op, fn, nbytes, tokens, bound="hbm"):
@@ -466,6 +474,13 @@ def run_parts(torch, lora, binding, synth, dev, stream, c3_sets, args, peak, pea
         for op in ops:
             lat = op in ("lora_group_by_slot", "lora_gather_shrink")
             add(cfg, op, lambda i, op=op: MF[op](m), by[op], m["T"], bound="latency" if lat else "hbm")
+        # the batch's schedule built once and reused by every op (how a serving
+        # engine runs the adapted layers of one batch)
+        add(cfg, "lora_build_schedule", lambda i: MF["lora_build_schedule"](m), by["lora_group_by_slot"], m["T"],
+            bound="latency")
+        MF["lora_build_schedule"](m)
+        for op in ("lora_shrink", "lora_expand", "lora_apply_linear"):
+            add(cfg, op + ".prebuilt_schedule", lambda i, op=op: MS[op](m), by[op], m["T"])
         del m
     del flush_buf
     torch.cuda.empty_cache()

@@ -87,9 +87,14 @@ typedef enum {
 } lora_op_t;
 
 /* Token -> adapter-slot addressing of the multi-adapter ops ([mstar lora.ops]
- * LoraAddressing, read as: one slot index per token).
+ * LoraAddressing, read as: one slot index per token, built once per batch).
  *   slots      device int32 [num_tokens]; slot(t)
  *   num_tokens T >= 0, num_slots S in [1, LORA_MAX_SLOTS], max_rank R in [1, LORA_MAX_RANK]
+ *   schedule   NULL, or the device schedule that lora_build_schedule made from
+ *              these slots, ranks, T, S and R (the grouping of the tokens by slot):
+ *              the ops then skip their own grouping step.  The caller keeps it
+ *              unchanged while ops that use it run, and rebuilds it whenever the
+ *              slots or the ranks change.
  * A token is ACTIVE when 0 <= slot(t) < S and 1 <= ranks[slot(t)] <= R.  An inactive
  * token (the zero adapter, an out-of-range slot or rank) contributes nothing: its
  * row of y is left untouched and its row of h is unspecified. */
@@ -98,6 +103,7 @@ typedef struct {
     int32_t num_tokens;
     int32_t num_slots;
     int32_t max_rank;
+    const void *schedule;
 } lora_addressing_t;
 
 /* Bytes of workspace that `op` needs for the given sizes (an upper bound that
@@ -266,6 +272,22 @@ LORA_API lora_status_t lora_backward_db_noalloc(lora_dtype_t dtype, int64_t M, i
 LORA_API lora_status_t lora_group_by_slot(const lora_addressing_t *addr, const int32_t *ranks,
                                  int32_t *counts, int32_t *perm, int32_t *num_active,
                                  void *ws, size_t ws_bytes, void *stream);
+
+/* --------------------------------------------------------------------------------
+ * lora_schedule_size / lora_build_schedule: the grouping step of the segmented
+ * ops (the stable sort of the active tokens by slot and the list of tiles of at
+ * most 128 tokens of one slot, as lora_group_by_slot defines it) done once, into
+ * a device buffer that lora_shrink, lora_expand and lora_apply_linear then reuse
+ * through addr->schedule ([mstar lora.ops]: the addressing of a batch is built
+ * once and serves every adapted layer; no host sync, no data-dependent shape).
+ *   schedule       device buffer of lora_schedule_size(T, S) bytes, 256-byte
+ *                  aligned, written by the call (addr->schedule is ignored).
+ * Errors: as lora_group_by_slot; a buffer that is NULL, misaligned or too small
+ * -> LORA_ERR_WORKSPACE.
+ * -------------------------------------------------------------------------------- */
+LORA_API size_t lora_schedule_size(int32_t num_tokens, int32_t num_slots);
+LORA_API lora_status_t lora_build_schedule(const lora_addressing_t *addr, const int32_t *ranks, void *schedule,
+                                  size_t schedule_bytes, void *stream);
 
 /* --------------------------------------------------------------------------------
  * lora_shrink:  h[t, i*R + j] = sum_k x[t,k] * a[slot(t)][i*R + j][k],  j < rank(slot(t))

@@ -25,7 +25,8 @@ STATUS = {0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_UNSUPPORTED", 3:
 EXPORTS = ["lora_workspace_size", "lora_forward", "lora_backward_dx_da", "lora_backward_db",
            "lora_group_by_slot", "lora_shrink", "lora_expand", "lora_apply_linear",
            "lora_gather_shrink", "lora_status_string", "lora_device_error", "lora_kernel_launches",
-           "lora_version", "lora_backward_db_noalloc", "lora_forward_h", "lora_backward", "lora_backward_ex"]
+           "lora_version", "lora_backward_db_noalloc", "lora_forward_h", "lora_backward", "lora_backward_ex",
+           "lora_schedule_size", "lora_build_schedule"]
 
 
 class LoraError(RuntimeError):
@@ -35,9 +36,11 @@ class LoraError(RuntimeError):
 
 
 class LoraAddressing(ctypes.Structure):
-    """lora_addressing_t: device slots pointer and the sizes T, S, R."""
+    """lora_addressing_t: device slots pointer, the sizes T, S, R, and an optional
+    prebuilt schedule (device pointer, or 0)."""
     _fields_ = [("slots", ctypes.c_void_p), ("num_tokens", ctypes.c_int32),
-                ("num_slots", ctypes.c_int32), ("max_rank", ctypes.c_int32)]
+                ("num_slots", ctypes.c_int32), ("max_rank", ctypes.c_int32),
+                ("schedule", ctypes.c_void_p)]
 
 
 _lib = None
@@ -69,6 +72,8 @@ def lib():
         "lora_backward_ex": (i32, [i32, i64, i64, i64, i32, P, i64, P, i64, P, i64, i64, P, i64, i64, P, i64,
                                    f32, P, i64, P, i64, i64, P, i64, i64, ctypes.c_uint32, P, sz, P]),
         "lora_group_by_slot": (i32, [AP, P, P, P, P, P, sz, P]),
+        "lora_schedule_size": (sz, [i32, i32]),
+        "lora_build_schedule": (i32, [AP, P, P, sz, P]),
         "lora_shrink": (i32, [AP, P, i64, i32, P, i64, P, i64, i64, P, i64, P, sz, P]),
         "lora_expand": (i32, [AP, P, P, P, i32, P, i64, P, i64, i64, i64, P, i64, P, sz, P]),
         "lora_apply_linear": (i32, [AP, P, P, P, i32, i64, P, i64, P, i64, i64, P, i64, i64, i64, P, i64,
@@ -228,9 +233,22 @@ def lora_backward_db(X, A, dY, scale, dB, ws=None, stream=None):
 
 
 # ----------------------------------------------------------------------------- multi adapter
-def _addr(slots, S, R):
+def _addr(slots, S, R, schedule=None):
     assert slots.dtype == torch.int32
-    return LoraAddressing(slots.data_ptr() if slots.numel() else 0, slots.numel(), S, R)
+    return LoraAddressing(slots.data_ptr() if slots.numel() else 0, slots.numel(), S, R,
+                          schedule.data_ptr() if schedule is not None and schedule.numel() else 0)
+
+
+def lora_build_schedule(slots, ranks, R, stream=None):
+    """The grouping of a batch's tokens by slot, built once on the device (a
+    uint8 tensor) for the shrink / expand / apply_linear calls of that batch."""
+    S, T = ranks.numel(), slots.numel()
+    n = lib().lora_schedule_size(T, S)
+    sched = torch.empty(max(n, 1), dtype=torch.uint8, device=slots.device)
+    ad = _addr(slots, S, R)
+    _check(lib().lora_build_schedule(ctypes.byref(ad), _ptr(ranks), _ptr(sched), sched.numel(), _stream(stream)),
+           "lora_build_schedule")
+    return sched
 
 
 def lora_group_by_slot(slots, ranks, R, counts, perm, num_active, ws=None, stream=None):
@@ -244,7 +262,7 @@ def lora_group_by_slot(slots, ranks, R, counts, perm, num_active, ws=None, strea
     _check(st, "lora_group_by_slot")
 
 
-def lora_shrink(x, a, slots, ranks, R, h, num_slices=1, ws=None, stream=None):
+def lora_shrink(x, a, slots, ranks, R, h, num_slices=1, ws=None, stream=None, schedule=None):
     """h[t, i*R + j] = x[t] . a[slot(t), i*R + j] for j < rank (h fp32 [T, n*R])."""
     T, IN = x.shape
     S = ranks.numel()
@@ -252,7 +270,7 @@ def lora_shrink(x, a, slots, ranks, R, h, num_slices=1, ws=None, stream=None):
     assert a.stride(2) == 1
     if ws is None:
         ws = workspace(OP_SHRINK, LORA_BF16, T, IN, num_slices * R, R, S, device=x.device)
-    ad = _addr(slots, S, R)
+    ad = _addr(slots, S, R, schedule)
     st = lib().lora_shrink(ctypes.byref(ad), _ptr(ranks), IN, num_slices, _ptr(x), x.stride(0), _ptr(a),
                            a.stride(0), a.stride(1), _ptr(h), h.stride(0), *_ws_args(ws), _stream(stream))
     _check(st, "lora_shrink")
@@ -264,7 +282,7 @@ def _slices(out_slices):
     return (ctypes.c_int32 * n)(*[int(v) for v in out_slices]), n
 
 
-def lora_expand(h, b, slots, ranks, scalings, y, out_slices, R, ws=None, stream=None):
+def lora_expand(h, b, slots, ranks, scalings, y, out_slices, R, ws=None, stream=None, schedule=None):
     """y[t, slice i] += scalings[slot] * h[t, slice i] @ b[slot, slice i]^T (b [S, O, R])."""
     T = y.shape[0]
     S = ranks.numel()
@@ -273,7 +291,7 @@ def lora_expand(h, b, slots, ranks, scalings, y, out_slices, R, ws=None, stream=
     assert b.dim() == 3 and b.shape[0] == S and b.shape[1] == O and b.shape[2] == R
     if ws is None:
         ws = workspace(OP_EXPAND, LORA_BF16, T, 0, O, R, S, device=y.device)
-    ad = _addr(slots, S, R)
+    ad = _addr(slots, S, R, schedule)
     st = lib().lora_expand(ctypes.byref(ad), _ptr(ranks), _ptr(scalings), osl, n, _ptr(h), h.stride(0),
                            _ptr(b), b.stride(0), b.stride(1), b.stride(2), _ptr(y), y.stride(0),
                            *_ws_args(ws), _stream(stream))
@@ -281,7 +299,7 @@ def lora_expand(h, b, slots, ranks, scalings, y, out_slices, R, ws=None, stream=
     return y
 
 
-def lora_apply_linear(x, a, b, slots, ranks, scalings, y, out_slices, R, ws=None, stream=None):
+def lora_apply_linear(x, a, b, slots, ranks, scalings, y, out_slices, R, ws=None, stream=None, schedule=None):
     """Fused shrink + expand into y."""
     T, IN = x.shape
     S = ranks.numel()
@@ -291,7 +309,7 @@ def lora_apply_linear(x, a, b, slots, ranks, scalings, y, out_slices, R, ws=None
     assert b.dim() == 3 and b.shape[0] == S and b.shape[1] == O and b.shape[2] == R
     if ws is None:
         ws = workspace(OP_APPLY_LINEAR, LORA_BF16, T, IN, O, R, S, device=x.device)
-    ad = _addr(slots, S, R)
+    ad = _addr(slots, S, R, schedule)
     st = lib().lora_apply_linear(ctypes.byref(ad), _ptr(ranks), _ptr(scalings), osl, n, IN, _ptr(x),
                                  x.stride(0), _ptr(a), a.stride(0), a.stride(1), _ptr(b), b.stride(0),
                                  b.stride(1), b.stride(2), _ptr(y), y.stride(0), *_ws_args(ws),

@@ -327,6 +327,7 @@ lora_status_t lora_backward_db(lora_dtype_t dtype, int64_t M, int64_t K, int64_t
 // ----------------------------------------------------------------------------- multi adapter
 static lora_status_t check_addr(const lora_addressing_t *addr, const int32_t *ranks) {
   if (addr == nullptr) return LORA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(addr->schedule) & 255u) != 0) return LORA_ERR_ALIGNMENT;
   if (addr->num_tokens < 0 || addr->num_slots < 1 || addr->max_rank < 1) return LORA_ERR_INVALID_ARG;
   if (addr->num_slots > LORA_MAX_SLOTS || addr->max_rank > LORA_MAX_RANK) return LORA_ERR_UNSUPPORTED;
   if (addr->num_tokens > 0 && (addr->slots == nullptr || ranks == nullptr)) return LORA_ERR_INVALID_ARG;
@@ -355,6 +356,18 @@ lora_status_t lora_group_by_slot(const lora_addressing_t *addr, const int32_t *r
   LORA_TRY(check_ws(ws, ws_bytes, multi_ws_bytes(LORA_OP_GROUP_BY_SLOT, addr->num_tokens, 0, 0, addr->max_rank,
                                                  addr->num_slots)));
   return group_by_slot(*addr, ranks, counts, perm, num_active, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+size_t lora_schedule_size(int32_t num_tokens, int32_t num_slots) {
+  if (num_tokens < 0 || num_slots < 1 || num_slots > LORA_MAX_SLOTS) return 0;
+  return schedule_bytes(num_tokens, num_slots);
+}
+
+lora_status_t lora_build_schedule(const lora_addressing_t *addr, const int32_t *ranks, void *schedule,
+                                  size_t schedule_bytes_, void *stream) {
+  LORA_TRY(check_addr(addr, ranks));
+  LORA_TRY(check_ws(schedule, schedule_bytes_, schedule_bytes(addr->num_tokens, addr->num_slots)));
+  return build_schedule(*addr, ranks, schedule, schedule_bytes_, (cudaStream_t)stream);
 }
 
 lora_status_t lora_shrink(const lora_addressing_t *addr, const int32_t *ranks, int64_t in, int32_t num_slices,

@@ -1140,7 +1140,13 @@ MArgs margs(const MultiArgs &m, const SchedPtrs &sp) {
   return a;
 }
 
+// The schedule of the call: the caller's prebuilt one (no launch), else built
+// into the workspace by the grouping kernel.
 lora_status_t schedule(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, cudaStream_t st) {
+  if (m.addr.schedule != nullptr) {
+    WsCarver pre(const_cast<void *>(m.addr.schedule), sched_bytes(m.addr.num_tokens, m.addr.num_slots));
+    return carve_sched(pre, m.addr.num_tokens, m.addr.num_slots, sp) ? LORA_OK : LORA_ERR_WORKSPACE;
+  }
   if (!carve_sched(c, m.addr.num_tokens, m.addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
   return launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st);
 }
@@ -1184,8 +1190,17 @@ MtArgs mt_args(const MultiArgs &m, const SchedPtrs &sp) {
 
 // Schedule (grouping kernel, which also zeroes the tickets), carving the counters.
 lora_status_t tc_schedule(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, MtArgs &a, cudaStream_t st) {
-  if (!carve_sched(c, m.addr.num_tokens, m.addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
   const int nc = max_tiles(m.addr.num_tokens, m.addr.num_slots) + 1;
+  if (m.addr.schedule != nullptr) {
+    LORA_TRY(schedule(m, c, sp, st));
+    int *cnt = (int *)c.take((size_t)nc * 4);
+    if (!cnt) return LORA_ERR_WORKSPACE;
+    LORA_CUDA(cudaMemsetAsync(cnt, 0, (size_t)nc * 4, st));
+    a = mt_args(m, sp);
+    a.counters = cnt;
+    return LORA_OK;
+  }
+  if (!carve_sched(c, m.addr.num_tokens, m.addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
   int *cnt = (int *)c.take((size_t)nc * 4);
   if (!cnt) return LORA_ERR_WORKSPACE;
   LORA_TRY(launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st, cnt, nc));
@@ -1210,6 +1225,17 @@ lora_status_t schedule_then_shrink(const MultiArgs &m, WsCarver &c, SchedPtrs &s
 }
 
 }  // namespace
+
+size_t schedule_bytes(int64_t T, int S) { return T > 0 ? sched_bytes(T, S) : 0; }
+
+lora_status_t build_schedule(const lora_addressing_t &addr, const int32_t *ranks, void *sched, size_t bytes,
+                             cudaStream_t st) {
+  if (addr.num_tokens == 0) return LORA_OK;
+  WsCarver c(sched, bytes);
+  SchedPtrs sp;
+  if (!carve_sched(c, addr.num_tokens, addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
+  return launch_group(addr, ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st);
+}
 
 size_t multi_ws_bytes(int op, int64_t T, int64_t in, int64_t O, int R, int S) {
   (void)in;

@@ -26,6 +26,9 @@ struct MultiArgs {
 };
 
 size_t multi_ws_bytes(int op, int64_t T, int64_t in, int64_t O, int R, int S);
+size_t schedule_bytes(int64_t T, int S);
+lora_status_t build_schedule(const lora_addressing_t &addr, const int32_t *ranks, void *sched, size_t bytes,
+                             cudaStream_t st);
 
 lora_status_t group_by_slot(const lora_addressing_t &addr, const int32_t *ranks, int32_t *counts, int32_t *perm,
                             int32_t *num_active, void *ws, size_t ws_bytes, cudaStream_t st);

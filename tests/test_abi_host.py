@@ -17,7 +17,7 @@ def L():
 
 def test_every_declared_symbol_is_exported(L):
     declared = header_functions()
-    assert len(declared) == 17, declared
+    assert len(declared) == 19, declared
     assert sorted(B.EXPORTS) == declared
     for name in declared:
         assert hasattr(L, name), name
@@ -147,3 +147,18 @@ def test_noalloc_argument_errors_come_before_the_size_check(L):
     assert nb(m=-1) == 1                  # negative size
     assert nb(rr=500) == 2                # rank above LORA_MAX_RANK
     assert nb() == 4                      # valid but larger than the scratch array
+
+
+def test_schedule_argument_errors(L):
+    """lora_build_schedule checks its buffer; a prebuilt schedule in the
+    addressing must be 256-byte aligned (checked before any launch)."""
+    slots = ctypes.c_void_p(0x20000)
+    assert L.lora_schedule_size(4096, 32) > 4096 * 4
+    assert L.lora_schedule_size(0, 32) == 0 and L.lora_schedule_size(10, 0) == 0
+    ad = B.LoraAddressing(slots.value, 4096, 32, 64, 0)
+    P = ctypes.byref
+    assert L.lora_build_schedule(P(ad), FAKE, NULL, 0, S0) == 4
+    assert L.lora_build_schedule(P(ad), FAKE, MIS, 1 << 20, S0) == 4
+    assert L.lora_build_schedule(None, FAKE, FAKE, 1 << 20, S0) == 1
+    bad = B.LoraAddressing(slots.value, 4096, 32, 64, 0x10010)   # not 256-byte aligned
+    assert L.lora_shrink(P(bad), FAKE, 64, 1, FAKE, 64, FAKE, 512, 64, FAKE, 64, NULL, 0, S0) == 3

@@ -313,3 +313,49 @@ def test_c5_gather_every_token():
         assert np.array_equal(got[toks][m[toks]], one[m[toks]])
         checked += len(toks)
     assert checked == T
+
+
+@pytest.mark.parametrize("T,IN,osl,S,R,ch,layout", [CASES[3], CASES[4], CASES[8], CASES[10], CASES[11]])
+def test_prebuilt_schedule_same_bits(T, IN, osl, S, R, ch, layout):
+    """A schedule built once (lora_build_schedule) and passed in the addressing
+    gives bit-for-bit the results of the ops that group the tokens themselves,
+    and the same y as the oracle."""
+    w = workload(T, IN, osl, S, R, ch, layout, seed=T + 5, bad_slots=0.05)
+    n = len(osl)
+    sched = lora.lora_build_schedule(w["slots"], w["ranks"], R)
+    outs = {}
+    for tag, sc in (("own", None), ("pre", sched)):
+        h = torch.full((T, n * R), float("nan"), dtype=torch.float32, device=DEV)
+        lora.lora_shrink(w["x"], w["a"], w["slots"], w["ranks"], R, h, num_slices=n, schedule=sc)
+        y1 = w["y0"].clone()
+        lora.lora_expand(h, w["b"], w["slots"], w["ranks"], w["scalings"], y1, osl, R, schedule=sc)
+        y2 = w["y0"].clone()
+        lora.lora_apply_linear(w["x"], w["a"], w["b"], w["slots"], w["ranks"], w["scalings"], y2, osl, R,
+                               schedule=sc)
+        torch.cuda.synchronize()
+        outs[tag] = (h, y1, y2)
+    assert lora.lora_device_error() == 0
+    m = torch.from_numpy(spec_mask(w, n)).to(DEV)
+    assert torch.equal(outs["own"][0][m], outs["pre"][0][m])
+    assert torch.equal(outs["own"][1], outs["pre"][1]) and torch.equal(outs["own"][2], outs["pre"][2])
+    o = oracle_inputs(w)
+    ref = O.apply_linear(o["x"], o["a"], o["b"], o["slots"], o["ranks"], o["scal"], o["y0"], osl, R)
+    act = active_mask(w)
+    assert rel_err(f64(outs["pre"][2])[act], ref[act]) <= TOL_BF16
+
+
+def test_prebuilt_schedule_holds_the_grouping():
+    """The schedule's permutation and counts are lora_group_by_slot's (the oracle's stable sort)."""
+    w = workload(3000, 64, [64], 40, 64, [0, 8, 16, 64], "segments", seed=3, bad_slots=0.1)
+    sched = lora.lora_build_schedule(w["slots"], w["ranks"], 64)
+    torch.cuda.synchronize()
+    raw = sched.cpu().numpy()
+    S, T = 40, 3000
+    rc, rp = O.group_by_slot(w["slots"].cpu().numpy(), w["ranks"].cpu().numpy(), 64)
+    # layout: header (256 B), counts [S] (256-byte rounded), perm [T]
+    header = raw[:256].view(np.int32)
+    counts = raw[256:256 + 4 * S].view(np.int32)
+    off = 256 + ((4 * S + 255) // 256) * 256
+    perm = raw[off:off + 4 * T].view(np.int32)
+    assert header[0] == len(rp)
+    assert counts.tolist() == rc.tolist() and perm[:len(rp)].tolist() == rp.tolist()
