@@ -10,7 +10,8 @@ a CUDA implementation that calls the C ABI; there is no CPU kernel.
 
 `LoraLinearFn` / `lora_linear` is an autograd.Function over the single-adapter
 ops (NeMo AutoModel page "nemo_automodel.components._peft.lora_kernel":
-lora_forward_wrapper, lora_da_dx_update_wrapper, lora_db_update_wrapper):
+lora_forward_wrapper, lora_da_dx_update_wrapper, lora_db_update_wrapper), on
+the fused pair forward_h_ / backward_ex:
     out = base + scale * (x @ A) @ B
 with gradients dx = scale * dout @ B^T @ A^T, dA = scale * x^T @ (dout @ B^T),
 dB = scale * (x @ A)^T @ dout and dbase = dout.
@@ -111,21 +112,58 @@ def _(x, dout, A, B, scale):
             B.new_empty(B.shape, dtype=torch.float32)]
 
 
+@torch.library.custom_op(f"{NS}::forward_h_", mutates_args=("y",), device_types="cuda")
+def forward_h_(y: torch.Tensor, x: torch.Tensor, A: torch.Tensor, B: torch.Tensor, scale: float) -> torch.Tensor:
+    """y += scale * (x @ A) @ B in place; returns h = x @ A (fp32) for backward_ex."""
+    h = torch.empty((x.shape[0], A.shape[1]), dtype=torch.float32, device=x.device)
+    binding.lora_forward_h(x, A, B, y, scale, h)
+    return h
+
+
+@forward_h_.register_fake
+def _(y, x, A, B, scale):
+    return x.new_empty((x.shape[0], A.shape[1]), dtype=torch.float32)
+
+
+@torch.library.custom_op(f"{NS}::backward_ex", mutates_args=(), device_types="cuda")
+def backward_ex(x: torch.Tensor, dout: torch.Tensor, A: torch.Tensor, B: torch.Tensor, h: torch.Tensor,
+                scale: float, grads_in_input_dtype: bool) -> List[torch.Tensor]:
+    """(dx, dA, dB) in one call from the h that forward_h_ saved (x is read
+    once); dA and dB in x's dtype when grads_in_input_dtype, else fp32."""
+    gdt = x.dtype if grads_in_input_dtype else torch.float32
+    dx = torch.empty_like(x)
+    dA = torch.empty(A.shape, dtype=gdt, device=x.device)
+    dB = torch.empty(B.shape, dtype=gdt, device=x.device)
+    flags = binding.BWD_GRAD_INPUT_DTYPE if grads_in_input_dtype else 0
+    binding.lora_backward_ex(x, dout, A, B, h, scale, dx, dA, dB, flags=flags)
+    return [dx, dA, dB]
+
+
+@backward_ex.register_fake
+def _(x, dout, A, B, h, scale, grads_in_input_dtype):
+    gdt = x.dtype if grads_in_input_dtype else torch.float32
+    return [torch.empty_like(x), A.new_empty(A.shape, dtype=gdt), B.new_empty(B.shape, dtype=gdt)]
+
+
 class LoraLinearFn(torch.autograd.Function):
-    """out = base + scale * (x @ A) @ B on the GPU kernels, with their backward."""
+    """out = base + scale * (x @ A) @ B on the GPU kernels: the forward saves
+    h = x @ A, and the backward computes dx, dA and dB in one call from it (x is
+    read once), returning dA and dB in the parameters' dtype (rounded once from
+    the fp32 sums)."""
 
     @staticmethod
     def forward(ctx, x, A, B, base, scale):
         out = base.clone()
-        forward_(out, x, A, B, float(scale))
-        ctx.save_for_backward(x, A, B)
+        h = forward_h_(out, x, A, B, float(scale))
+        ctx.save_for_backward(x, A, B, h)
         ctx.scale = float(scale)
         return out
 
     @staticmethod
     def backward(ctx, dout):
-        x, A, B = ctx.saved_tensors
-        dx, dA, dB = backward(x, dout.contiguous(), A, B, ctx.scale)
+        x, A, B, h = ctx.saved_tensors
+        in_dtype = A.dtype == x.dtype and B.dtype == x.dtype
+        dx, dA, dB = backward_ex(x, dout.contiguous(), A, B, h, ctx.scale, in_dtype)
         return dx, dA.to(A.dtype), dB.to(B.dtype), dout, None
 
 

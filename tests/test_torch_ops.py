@@ -40,6 +40,11 @@ def test_fake_shapes_single_adapter():
         dx, dA, dB = torch.ops.lora_gb300.backward(x, dout, A, B, 2.0)
         assert dx.shape == x.shape and dA.shape == A.shape and dB.shape == B.shape
         assert dA.dtype == torch.float32 and dB.dtype == torch.float32
+        y = torch.empty((10, 40), dtype=torch.bfloat16)
+        h = torch.ops.lora_gb300.forward_h_(y, x, A, B, 2.0)
+        assert h.shape == (10, 8) and h.dtype == torch.float32
+        dx, dA, dB = torch.ops.lora_gb300.backward_ex(x, dout, A, B, h, 2.0, True)
+        assert dx.shape == x.shape and dA.dtype == torch.bfloat16 and dB.dtype == torch.bfloat16
 
 
 def test_no_cpu_kernel():
@@ -64,6 +69,9 @@ def test_opcheck_and_autograd_against_oracle():
     s = spec["s"]
     torch.library.opcheck(torch.ops.lora_gb300.forward_.default, (Y0.clone(), X, A, B, s))
     torch.library.opcheck(torch.ops.lora_gb300.backward.default, (X, dY, A, B, s))
+    h = torch.ops.lora_gb300.forward_h_(Y0.clone(), X, A, B, s)
+    torch.library.opcheck(torch.ops.lora_gb300.forward_h_.default, (Y0.clone(), X, A, B, s))
+    torch.library.opcheck(torch.ops.lora_gb300.backward_ex.default, (X, dY, A, B, h, s, True))
     Xg = X.clone().requires_grad_(True)
     Ag = A.clone().requires_grad_(True)
     Bg = B.clone().requires_grad_(True)
@@ -84,12 +92,30 @@ def test_opcheck_and_autograd_against_oracle():
 
 @pytest.mark.gpu
 def test_opcheck_multi_adapter():
+    """opcheck of the registrations, and the ops' results against the oracle."""
+    import numpy as np
     from lora_rank_adapter_gb300 import _build, synth
+    from oracle import oracle as O
     _build.build()
     spec = synth.multi_spec("multi_c4", T=200, IN=64, out_slices=[64, 32, 32], S=6, R=16,
                             rank_choices=[0, 8, 16])
     w = synth.make_multi(spec, seed=1, device="cuda:0", poison=False)
     h = torch.ops.lora_gb300.shrink(w["x"], w["a"], w["slots"], w["ranks"], 16, 3)
+    y = w["y0"].clone()
+    torch.ops.lora_gb300.apply_linear_(y, w["x"], w["a"], w["b"], w["slots"], w["ranks"], w["scalings"],
+                                       [64, 32, 32], 16)
+    torch.cuda.synchronize()
+    sl, rk = w["slots"].cpu().numpy(), w["ranks"].cpu().numpy()
+    sc = w["scalings"].double().cpu().numpy()
+    href = O.shrink(f64(w["x"]), f64(w["a"]), sl, rk, 16, 3)
+    act = np.array([0 <= v < 6 and 1 <= rk[v] <= 16 for v in sl])
+    spec_h = np.zeros(href.shape, bool)
+    for t in np.nonzero(act)[0]:
+        for i in range(3):
+            spec_h[t, i * 16:i * 16 + rk[sl[t]]] = True
+    assert rel_err(f64(h)[spec_h], href[spec_h]) <= TOL_F32
+    yref = O.apply_linear(f64(w["x"]), f64(w["a"]), f64(w["b"]), sl, rk, sc, f64(w["y0"]), [64, 32, 32], 16)
+    assert rel_err(f64(y)[act], yref[act]) <= TOL_BF16
     torch.library.opcheck(torch.ops.lora_gb300.shrink.default, (w["x"], w["a"], w["slots"], w["ranks"], 16, 3),
                           test_utils=("test_schema", "test_faketensor", "test_autograd_registration"))
     torch.library.opcheck(torch.ops.lora_gb300.expand_.default,
