@@ -28,7 +28,7 @@
 #include "common.cuh"
 #include "host_common.h"
 #include "multi.h"
-#include "multi_tc.h"
+#include "decode.h"
 
 namespace lora {
 
@@ -138,47 +138,43 @@ __device__ __forceinline__ unsigned same_key_lanes(int key) {
 // slot are listed in slot order.  Slots are read in batches of 8 per lane so
 // their loads overlap.
 // =============================================================================
-__device__ __forceinline__ void block_scan2(int a, int b, int &ea, int &eb, int &ta, int &tb, int *sh) {
+// Exclusive block-wide scan of three values per thread: e[k] the sum over the
+// threads before this one, t[k] the block total.  sh: 3 * 64 + 3 ints.
+__device__ __forceinline__ void block_scan3(const int (&v)[3], int (&e)[3], int (&t)[3], int *sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int ia = a, ib = b;
+  int in[3] = {v[0], v[1], v[2]};
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int va = __shfl_up_sync(0xffffffffu, ia, o), vb = __shfl_up_sync(0xffffffffu, ib, o);
-    if (lane >= o) {
-      ia += va;
-      ib += vb;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int x = __shfl_up_sync(0xffffffffu, in[k], o);
+      if (lane >= o) in[k] += x;
     }
   }
-  if (lane == 31) {
-    sh[warp] = ia;
-    sh[32 + warp] = ib;
-  }
+  if (lane == 31)
+#pragma unroll
+    for (int k = 0; k < 3; ++k) sh[32 * k + warp] = in[k];
   __syncthreads();
   if (warp == 0) {
-    int va = lane < nw ? sh[lane] : 0, vb = lane < nw ? sh[32 + lane] : 0;
-    int sa = va, sb = vb;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int xa = __shfl_up_sync(0xffffffffu, sa, o), xb = __shfl_up_sync(0xffffffffu, sb, o);
-      if (lane >= o) {
-        sa += xa;
-        sb += xb;
+    for (int k = 0; k < 3; ++k) {
+      const int w = lane < nw ? sh[32 * k + lane] : 0;
+      int sc = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, sc, o);
+        if (lane >= o) sc += x;
       }
-    }
-    if (lane < nw) {
-      sh[64 + lane] = sa - va;
-      sh[96 + lane] = sb - vb;
-    }
-    if (lane == 31) {
-      sh[128] = sa;
-      sh[129] = sb;
+      if (lane < nw) sh[96 + 32 * k + lane] = sc - w;
+      if (lane == 31) sh[192 + k] = sc;
     }
   }
   __syncthreads();
-  ea = sh[64 + warp] + ia - a;
-  eb = sh[96 + warp] + ib - b;
-  ta = sh[128];
-  tb = sh[129];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    e[k] = sh[96 + 32 * k + warp] + in[k] - v[k];
+    t[k] = sh[192 + k];
+  }
   __syncthreads();
 }
 
@@ -199,7 +195,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
   int *srank = gsm + nw * S;       // [S]
   int *scnt = srank + S;           // [S] active tokens of each slot
   int *sbase = scnt + S;           // [S] first position of each slot in the permutation
-  int *sh = sbase + S;             // scan scratch (160 ints)
+  int *sh = sbase + S;             // scan scratch (224 ints)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
   // the tickets of the kernel that follows start at zero
@@ -249,26 +245,34 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
     if (lane == 31) scnt[s] = inc;
   }
   __syncthreads();
-  int run = 0, trun = 0;
+  // tile t = (slot, start, len, rows): rows = the sum over the tiles before t of
+  // round8(rank), the adapter rows per slice that a contraction over those
+  // tiles reads (the cost weights of the stream-K shrink)
+  int run = 0, trun = 0, rrun = 0;
   for (int c0 = 0; c0 < S; c0 += blockDim.x) {
     const int s = c0 + threadIdx.x;
     const int cnt = s < S ? scnt[s] : 0;
     const int nt = (cnt + bmt - 1) / bmt;
-    int ec, et, tc, tt;
-    block_scan2(cnt, nt, ec, et, tc, tt, sh);
+    const int r8 = cnt > 0 ? (srank[s] + 7) & ~7 : 0;
+    const int v[3] = {cnt, nt, nt * r8};
+    int e[3], tot[3];
+    block_scan3(v, e, tot, sh);
     if (s < S) {
-      const int base = run + ec, tb = trun + et;
+      const int base = run + e[0], tb = trun + e[1], rb = rrun + e[2];
       counts_out[s] = cnt;
       sbase[s] = base;
-      for (int i = 0; i < nt; ++i) tiles[tb + i] = make_int4(s, base + i * bmt, min(bmt, cnt - i * bmt), 0);
+      for (int i = 0; i < nt; ++i)
+        tiles[tb + i] = make_int4(s, base + i * bmt, min(bmt, cnt - i * bmt), rb + i * r8);
     }
-    run += tc;
-    trun += tt;
+    run += tot[0];
+    trun += tot[1];
+    rrun += tot[2];
   }
   if (threadIdx.x == 0) {
     *num_active_out = run;
     header[0] = run;
     header[1] = trun;
+    header[2] = rrun;
   }
   __syncthreads();
   for (int t0 = t_lo; t0 < t_hi; t0 += 32 * GU) {
@@ -809,66 +813,89 @@ __global__ void __launch_bounds__(ExCfg<RP>::THREADS, RP >= 128 ? 2 : 3)
 // =============================================================================
 // expand_decode_kernel: the expand for tiles of a few tokens (decode batches,
 // where every token may carry its own adapter).  The work is streaming the
-// slots' b rows; a block takes one tile and 256 output columns of one slice,
-// each thread one output column c: it loads b[slot][c][0 .. rank) once (16-byte
-// loads) and for each token t of the tile adds scal * sum_j h[t][i R + j] b[c][j]
-// into y[t][c] (the warp's 32 columns of a token row are one coalesced access).
-// Columns j >= rank of h and b are never read.
+// slots' b rows b[slot][c][0 .. rank).  A block takes one tile, one slice i and
+// a range of output columns holding 2048 sixteen-byte pieces of b: a column's
+// ceil(rank / 8) pieces sit in P consecutive lanes (P = that count rounded up
+// to a power of two), so every block reads about the same bytes whatever the
+// rank, and a thread keeps eight pieces in flight.  A lane multiplies its piece
+// by the matching eight entries of each token's h row (held in shared memory),
+// the P lanes of a column add their partial sums with shuffles, and the first
+// of them adds scal * sum into y[t][c].  Columns j >= rank of h and b are never
+// used (the pieces are masked past the rank).
 // =============================================================================
-constexpr int DX_COLS = 256;   // output columns per block
+constexpr int DX_THREADS = 256;
+constexpr int DX_PIECES = 8;    // sixteen-byte pieces of b per thread
+constexpr int DX_BLOCK_PIECES = DX_THREADS * DX_PIECES;
+
+// Columns a block covers for pieces-per-column P.
+__host__ __device__ __forceinline__ int dx_cols(int P) { return DX_BLOCK_PIECES / P; }
 
 template <int RP>
-__global__ void __launch_bounds__(DX_COLS) expand_decode_kernel(MArgs p) {
-  extern __shared__ float hs[];   // [len][RP] of the tile's h rows (slice i)
+__global__ void __launch_bounds__(DX_THREADS, 4) expand_decode_kernel(MArgs p) {
+  extern __shared__ float hs[];   // [len][RP] of the tile's h rows (slice i), then [len] token rows
   pdl_wait();
   const int nblk = p.ngroups;     // blocks per tile (over all slices)
   const int tile = blockIdx.x / nblk, bi = blockIdx.x % nblk;
   if (tile >= p.header[1]) return;
-  // block -> slice i and its first column
+  // block -> slice i and its index inside the slice (the host sized the grid
+  // for P = RP / 8, the most pieces a column can have)
   int i = 0, left = bi;
   for (; i < p.n; ++i) {
-    const int nb = (p.off[i + 1] - p.off[i] + DX_COLS - 1) / DX_COLS;
+    const int nb = (p.off[i + 1] - p.off[i] + dx_cols(RP / 8) - 1) / dx_cols(RP / 8);
     if (left < nb) break;
     left -= nb;
   }
   if (i >= p.n) return;
   const int4 td = p.tiles[tile];
   const int slot = td.x, start = td.y, len = td.z;
-  const int rank = p.ranks[slot];
-  const float sc = p.scal[slot];
-  for (int e = threadIdx.x; e < len * RP; e += blockDim.x) {
+  const int rank = min(p.ranks[slot], RP);
+  const int npc = (rank + 7) >> 3;
+  int lgP = 0;
+  while ((1 << lgP) < npc) ++lgP;
+  const int P = 1 << lgP;
+  const int width = p.off[i + 1] - p.off[i];
+  const int col0 = left * dx_cols(P);
+  if (col0 >= width) return;   // fewer pieces per column: fewer blocks cover the slice
+  const int tid = threadIdx.x, pc = tid & (P - 1);
+  // b pieces first (their loads in flight while h is staged)
+  const __nv_bfloat16 *bs = p.b + (int64_t)slot * p.sb_slot + (int64_t)p.off[i] * p.sb_row;
+  uint4 w[DX_PIECES];
+#pragma unroll
+  for (int k = 0; k < DX_PIECES; ++k) {
+    const int c = col0 + ((k * DX_THREADS + tid) >> lgP);
+    w[k] = c < width && pc < npc ? *reinterpret_cast<const uint4 *>(bs + (int64_t)c * p.sb_row + pc * 8)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+  }
+  int *rows = reinterpret_cast<int *>(hs + len * RP);
+  for (int e = tid; e < len * RP; e += DX_THREADS) {
     const int t = e / RP, j = e % RP;
     hs[e] = j < rank ? p.h[(int64_t)p.perm[start + t] * p.ldh + (int64_t)i * p.R + j] : 0.f;
   }
+  for (int t = tid; t < len; t += DX_THREADS) rows[t] = p.perm[start + t];
+  const float sc = p.scal[slot];
+  // entries past the rank in this lane's pieces may hold anything: a mask per
+  // 32-bit word (two entries) clears them
+  const int tail = rank - pc * 8;
+  const uint32_t m0 = tail >= 2 ? ~0u : tail == 1 ? 0xffffu : 0u, m1 = tail >= 4 ? ~0u : tail == 3 ? 0xffffu : 0u,
+                 m2 = tail >= 6 ? ~0u : tail == 5 ? 0xffffu : 0u, m3 = tail >= 8 ? ~0u : tail == 7 ? 0xffffu : 0u;
   __syncthreads();
-  const int c = p.off[i] + left * DX_COLS + threadIdx.x;
-  if (c >= p.off[i + 1]) return;
-  // b[slot][c][0 .. rank): rank16 / 8 sixteen-byte loads, the padding masked
-  const __nv_bfloat16 *br = p.b + (int64_t)slot * p.sb_slot + (int64_t)c * p.sb_row;
-  float bv[RP];
 #pragma unroll
-  for (int j = 0; j < RP; j += 8) {
-    if (j < rank) {
-      const uint4 w = *reinterpret_cast<const uint4 *>(br + j);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = unpack_bf16(ww[e]);
-        bv[j + 2 * e] = j + 2 * e < rank ? f.x : 0.f;
-        bv[j + 2 * e + 1] = j + 2 * e + 1 < rank ? f.y : 0.f;
+  for (int k = 0; k < DX_PIECES; ++k) {
+    const float2 b0 = unpack_bf16(w[k].x & m0), b1 = unpack_bf16(w[k].y & m1), b2 = unpack_bf16(w[k].z & m2),
+                 b3 = unpack_bf16(w[k].w & m3);
+    const int c = col0 + ((k * DX_THREADS + tid) >> lgP);
+    const bool store = pc == 0 && c < width;
+    for (int t = 0; t < len; ++t) {
+      const float4 h0 = *reinterpret_cast<const float4 *>(hs + t * RP + pc * 8);
+      const float4 h1 = *reinterpret_cast<const float4 *>(hs + t * RP + pc * 8 + 4);
+      float acc = h0.x * b0.x + h0.y * b0.y + h0.z * b1.x + h0.w * b1.y + h1.x * b2.x + h1.y * b2.y +
+                  h1.z * b3.x + h1.w * b3.y;
+      for (int o = 1; o < P; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (store) {
+        __nv_bfloat16 *yp = p.y + (int64_t)rows[t] * p.ldy + p.off[i] + c;
+        *yp = __float2bfloat16_rn(__bfloat162float(*yp) + sc * acc);
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) bv[j + e] = 0.f;
     }
-  }
-  for (int t = 0; t < len; ++t) {
-    const float *ht = hs + t * RP;
-    float acc = 0.f;
-#pragma unroll
-    for (int j = 0; j < RP; ++j) acc += ht[j] * bv[j];
-    __nv_bfloat16 *yp = p.y + (int64_t)p.perm[start + t] * p.ldy + c;
-    *yp = __float2bfloat16_rn(__bfloat162float(*yp) + sc * acc);
   }
   pdl_launch_dependents();
 }
@@ -912,10 +939,17 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t *__restrict__
 
 
 // ----------------------------------------------------------------------------- host side
+// Decode batches: at most four tokens per slot on average.
+bool decode_shape(int64_t T, int S) { return T <= 4 * (int64_t)S; }
+
 namespace {
 
-// Tiles of at most TC_M tokens of one slot: at most one partial tile per slot.
-int max_tiles(int64_t T, int S) { return (int)(ceil_div(T, TC_M) + std::min<int64_t>(S, T)); }
+// Tokens per tile: decode batches (a few tokens per slot) are cut into tiles of
+// at most four tokens for the CUDA-core shrink and expand, prefill batches into
+// tiles of at most TC_M tokens for the tiled kernels.
+int tile_tokens(int64_t T, int S) { return decode_shape(T, S) ? kDecTokens : TC_M; }
+// At most one partial tile per slot.
+int max_tiles(int64_t T, int S) { return (int)(ceil_div(T, tile_tokens(T, S)) + std::min<int64_t>(S, T)); }
 
 struct SchedPtrs {
   int *header, *counts;
@@ -947,10 +981,11 @@ lora_status_t launch_group(const lora_addressing_t &ad, const int32_t *ranks, in
   // slots s = w, w + nw, ...): at most 8 slots per warp
   const int64_t want = std::max<int64_t>(ceil_div(ad.num_tokens, LORA_GROUP_TOKENS_PER_WARP), ceil_div(S, 8));
   nw = std::min<int64_t>({nw, 32, std::max<int64_t>(1, want)});
-  const size_t smem = (size_t)(nw * S + 3 * S + 160) * 4;
+  const size_t smem = (size_t)(nw * S + 3 * S + 224) * 4;
   LORA_CUDA(ensure_smem((const void *)group_kernel, smem));
   LORA_CUDA(launch(group_kernel, dim3(1), dim3(nw * 32), smem, st, 1, true, ad.slots, ad.num_tokens, S,
-                   ad.max_rank, ranks, counts, perm, num_active, header, tiles, (int)TC_M, zero, nzero));
+                   ad.max_rank, ranks, counts, perm, num_active, header, tiles, tile_tokens(ad.num_tokens, S), zero,
+                   nzero));
   return LORA_OK;
 }
 
@@ -1062,19 +1097,19 @@ lora_status_t launch_expand(MArgs a, int64_t T, cudaStream_t st) {
 template <int RP>
 lora_status_t launch_expand_decode(MArgs a, int64_t T, cudaStream_t st) {
   int nblk = 0;
-  for (int i = 0; i < a.n; ++i) nblk += (int)ceil_div(a.off[i + 1] - a.off[i], DX_COLS);
+  for (int i = 0; i < a.n; ++i) nblk += (int)ceil_div(a.off[i + 1] - a.off[i], dx_cols(RP / 8));
   if (nblk == 0) return LORA_OK;
   a.ngroups = nblk;
   const int64_t tiles = max_tiles(T, a.S);
-  const size_t smem = (size_t)TC_M * RP * 4;   // h rows of the largest tile
+  const size_t smem = (size_t)TC_M * (RP + 1) * 4;   // h rows and token rows of the largest tile
   LORA_CUDA(ensure_smem((const void *)expand_decode_kernel<RP>, smem));
-  LORA_CUDA(launch(expand_decode_kernel<RP>, dim3((unsigned)(tiles * nblk)), dim3(DX_COLS), smem, st, 1, true, a));
+  LORA_CUDA(
+      launch(expand_decode_kernel<RP>, dim3((unsigned)(tiles * nblk)), dim3(DX_THREADS), smem, st, 1, true, a));
   return LORA_OK;
 }
 
 // Decode batches (a few tokens per slot on average) stream the b rows on the
 // CUDA cores; prefill batches run the tiled expand.
-bool decode_shape(int64_t T, int S) { return T <= 4 * (int64_t)S; }
 
 lora_status_t dispatch_expand(const MArgs &a, int64_t T, cudaStream_t st) {
   if (decode_shape(T, a.S)) {
@@ -1169,10 +1204,9 @@ int shrink_cols(int64_t n_times_R, int R) {
   return (int)std::min<int64_t>(256, n_times_R > 0 ? n_times_R : (int64_t)LORA_MAX_SLICES * R);
 }
 
-MtArgs mt_args(const MultiArgs &m, const SchedPtrs &sp) {
-  MtArgs a{};
+DecArgs dec_args(const MultiArgs &m, const SchedPtrs &sp) {
+  DecArgs a{};
   a.ranks = m.ranks;
-  a.scal = m.scalings;
   a.header = sp.header;
   a.tiles = sp.tiles;
   a.perm = sp.perm;
@@ -1180,48 +1214,41 @@ MtArgs mt_args(const MultiArgs &m, const SchedPtrs &sp) {
   a.R = m.addr.max_rank;
   a.n = m.n;
   a.T = m.addr.num_tokens;
-  a.in = (int)m.in;
-  a.nk = (int)std::max<int64_t>(1, ceil_div(m.in, 64));
-  a.ncm = m.n * std::max(16, (int)round_up(m.addr.max_rank, 16));
+  a.nk = (int)std::max<int64_t>(1, ceil_div(m.in, 256));
   a.h = m.h;
   a.ldh = m.ldh;
   return a;
 }
 
-// Schedule (grouping kernel, which also zeroes the tickets), carving the counters.
-lora_status_t tc_schedule(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, MtArgs &a, cudaStream_t st) {
-  const int nc = max_tiles(m.addr.num_tokens, m.addr.num_slots) + 1;
-  if (m.addr.schedule != nullptr) {
-    LORA_TRY(schedule(m, c, sp, st));
-    int *cnt = (int *)c.take((size_t)nc * 4);
-    if (!cnt) return LORA_ERR_WORKSPACE;
-    LORA_CUDA(cudaMemsetAsync(cnt, 0, (size_t)nc * 4, st));
-    a = mt_args(m, sp);
-    a.counters = cnt;
-    return LORA_OK;
-  }
-  if (!carve_sched(c, m.addr.num_tokens, m.addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
-  int *cnt = (int *)c.take((size_t)nc * 4);
-  if (!cnt) return LORA_ERR_WORKSPACE;
-  LORA_TRY(launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st, cnt, nc));
-  a = mt_args(m, sp);
-  a.counters = cnt;
-  return LORA_OK;
-}
-
 // The schedule, then the shrink that suits the batch's shape: decode batches (a
-// few tokens per slot) split (tile, chunk) units evenly over a persistent grid;
-// prefill batches give each 128-token tile a cluster of CTAs.
+// few tokens per slot) split (tile, chunk) units by cost over a persistent grid
+// (their adapter rows read through a view that needs `in` a multiple of 64);
+// prefill batches, and the rest, give each tile a cluster of CTAs.
 lora_status_t schedule_then_shrink(const MultiArgs &m, WsCarver &c, SchedPtrs &sp, cudaStream_t st) {
-  if (!decode_shape(m.addr.num_tokens, m.addr.num_slots)) {
+  if (!decode_shape(m.addr.num_tokens, m.addr.num_slots) || m.in % 64 != 0) {
     MArgs a;
     return schedule_and_shrink(m, c, sp, &a, m.h, m.ldh, st);
   }
-  MtArgs a;
-  LORA_TRY(tc_schedule(m, c, sp, a, st));
-  a.part = (float *)c.take(multi_tc_part_bytes(m.n, m.addr.max_rank));
+  // the tickets (one per tile) start at zero: the grouping kernel clears them,
+  // or a memset when the caller's schedule is reused
+  const int nc = max_tiles(m.addr.num_tokens, m.addr.num_slots) + 1;
+  int *cnt = nullptr;
+  if (m.addr.schedule != nullptr) {
+    LORA_TRY(schedule(m, c, sp, st));
+    cnt = (int *)c.take((size_t)nc * 4);
+    if (!cnt) return LORA_ERR_WORKSPACE;
+    LORA_CUDA(cudaMemsetAsync(cnt, 0, (size_t)nc * 4, st));
+  } else {
+    if (!carve_sched(c, m.addr.num_tokens, m.addr.num_slots, sp)) return LORA_ERR_WORKSPACE;
+    cnt = (int *)c.take((size_t)nc * 4);
+    if (!cnt) return LORA_ERR_WORKSPACE;
+    LORA_TRY(launch_group(m.addr, m.ranks, sp.counts, sp.perm, sp.header, sp.header, sp.tiles, st, cnt, nc));
+  }
+  DecArgs a = dec_args(m, sp);
+  a.counters = cnt;
+  a.part = (float *)c.take(dec_part_bytes(m.n, m.addr.max_rank));
   if (!a.part) return LORA_ERR_WORKSPACE;
-  return shrink_tc_launch(a, m, m.addr.num_tokens, st);
+  return shrink_dec_launch(a, m, m.addr.num_tokens, st);
 }
 
 }  // namespace
@@ -1245,10 +1272,10 @@ size_t multi_ws_bytes(int op, int64_t T, int64_t in, int64_t O, int R, int S) {
   // shrink: O carries the width of h (num_slices * R), 0 when unknown
   if (op == LORA_OP_SHRINK) {
     const int nc = shrink_cols(O, R);
-    return sched_bytes(T, S) + tc_counter_bytes(T, S) + ws_round(multi_tc_part_bytes(1, nc));
+    return sched_bytes(T, S) + tc_counter_bytes(T, S) + ws_round(dec_part_bytes(1, nc));
   }
   if (op == LORA_OP_APPLY_LINEAR)
-    return sched_bytes(T, S) + tc_counter_bytes(T, S) + ws_round(multi_tc_part_bytes(1, shrink_cols(0, R))) +
+    return sched_bytes(T, S) + tc_counter_bytes(T, S) + ws_round(dec_part_bytes(1, shrink_cols(0, R))) +
            hbuf_bytes(T, R);
   return 0;
 }

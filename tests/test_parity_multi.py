@@ -108,6 +108,12 @@ CASES = [  # T, IN, out_slices, S, R, rank choices, layout
     (200, 520, [136], 64, 32, [0, 8, 16, 24, 32], "uniform"),
     (100, 72, [24, 40], 40, 16, [0, 8, 16], "uniform"),
     (9, 1000, [256], 9, 128, [0, 40, 128], "uniform"),
+    # decode-shaped, `in` a multiple of 64: a ragged last 256-column chunk, two and
+    # four 64-row blocks of adapter rows, one token over many slots
+    (200, 576, [136], 64, 32, [0, 8, 16, 24, 32], "uniform"),
+    (9, 1024, [256], 9, 128, [0, 40, 128], "uniform"),
+    (60, 320, [64, 64, 64, 64], 20, 64, [0, 8, 64], "uniform"),
+    (1, 8192, [64], 40, 64, [64], "uniform"),
 ]
 
 
@@ -315,7 +321,8 @@ def test_c5_gather_every_token():
     assert checked == T
 
 
-@pytest.mark.parametrize("T,IN,osl,S,R,ch,layout", [CASES[3], CASES[4], CASES[8], CASES[10], CASES[11]])
+@pytest.mark.parametrize("T,IN,osl,S,R,ch,layout", [CASES[3], CASES[4], CASES[8], CASES[10], CASES[11], CASES[12],
+                                                     CASES[14]])
 def test_prebuilt_schedule_same_bits(T, IN, osl, S, R, ch, layout):
     """A schedule built once (lora_build_schedule) and passed in the addressing
     gives bit-for-bit the results of the ops that group the tokens themselves,
