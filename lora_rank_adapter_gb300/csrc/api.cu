@@ -38,7 +38,8 @@ static EncodeTiledFn encode_fn() {
 }
 
 bool encode_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base, const uint64_t *dims,
-                 const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swz) {
+                 const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swz,
+                 CUtensorMapL2promotion promo) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t d[5], s[4];
@@ -50,7 +51,7 @@ bool encode_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void 
     if (i + 1 < rank) s[i] = strides_bytes[i];
   }
   CUresult r = fn(map, dt, (cuuint32_t)rank, const_cast<void *>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

@@ -38,12 +38,14 @@
 //           tile cut between CTAs leaves fp32 partial sums that the last CTA of
 //           the tile adds in CTA order (deterministic).
 #include <algorithm>
+#include <cstddef>
 #include <cstring>
 
 #include "common.cuh"
 #include "decode.h"
 #include "host_common.h"
 #include "multi.h"
+#include "tc_common.cuh"
 
 namespace lora {
 namespace dec {
@@ -73,11 +75,11 @@ __device__ __forceinline__ bool wait_lane0(uint64_t *bar, uint32_t parity) {
 
 // The cost split of the chunks over the grid.
 struct Split {
-  int nk, n, G;
+  int nk, n, tw, G;           // units per tile, adapter-row weight, token-row weight
   int64_t W;
   // first cost position of tile t (rows8 = its running sum of round8(rank))
   __device__ int64_t base(int t, int start, int rows8) const {
-    return (int64_t)nk * ((int64_t)n * rows8 + start + (int64_t)C0 * t);
+    return (int64_t)nk * ((int64_t)n * rows8 + (int64_t)tw * start + (int64_t)C0 * t);
   }
   // the CTA whose run holds the chunk at cost position cs
   __device__ int owner(int64_t cs) const {
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   Split sp;
   sp.nk = p.nk;
   sp.n = p.n;
+  sp.tw = 1;
   sp.W = (int64_t)p.nk * ((int64_t)p.n * p.header[2] + p.header[0] + (int64_t)C0 * ntiles);
   const int64_t wmax = (int64_t)p.n * ((p.R + 7) & ~7) + kDecTokens + C0, gw = sp.W / wmax;
   sp.G = gw < 1 ? 1 : gw < (int64_t)gridDim.x ? (int)gw : (int)gridDim.x;
@@ -353,6 +356,352 @@ __global__ void __launch_bounds__(NTHR, 1)
   pdl_launch_dependents();
 }
 
+// ============================================================================= expand
+// Units (tile, 256 output columns of slice i) are split over the grid by cost.
+// HBM serves whole 128-byte lines, so a unit's 256 rows of b cost the same
+// whatever the slot's rank (min(R, 64) entries of each row are fetched): a unit
+// weighs that fixed b cost + two token rows of y + C0.  No unit shares an
+// output with another, so a CTA's run needs no reduction.  A stage holds up to
+// q units of one tile and slice: per unit the tile's y row segments (one
+// 256-column box per token, updated in place) and round8(rank) rank entries of
+// 256 rows of b as boxes of 64, 32, 16 and 8 entries (one TMA row request per
+// box row; swizzled so that the fragment loads hit distinct banks).  Compute
+// warp w takes the 8-column groups w, w + 8, w + 16, w + 24 of each unit:
+// mma.sync with A = the tile's h rows (bf16 high part and residual, so that h
+// keeps about fp32 precision) and B = the b pieces (entries past the rank
+// masked: b may hold anything there), then y += scal * D in shared memory;
+// after a barrier one thread stores the updated rows with TMA stores.
+constexpr int ECB = 256;                     // output columns of a unit
+constexpr int EYB = ECB * 2;                 // bytes of a y row segment
+constexpr int EYA = kDecTokens * EYB;        // y area of a unit
+constexpr int EGB = ECB * 16;                // one box of b: 256 rows x 8 entries
+
+struct ExpTile {
+  int slot, start, len, rank, r8, ng, q;
+};
+__device__ __forceinline__ ExpTile exp_tile(const DecExpArgs &p, int tile, int ntiles) {
+  const int4 td = p.tiles[tile];
+  const int rows_next = tile + 1 < ntiles ? p.tiles[tile + 1].w : p.header[2];
+  ExpTile t;
+  t.slot = td.x;
+  t.start = td.y;
+  t.len = td.z;
+  t.r8 = rows_next - td.w;
+  t.rank = min(p.ranks[t.slot], t.r8);
+  t.ng = t.r8 / 8;
+  t.q = max(1, min(kMaxQ, STAGE / (EYA + t.ng * EGB)));
+  return t;
+}
+// Box k of the round8(rank) entries (64, 32, 16 or 8 wide, largest first): its
+// width index (0: 8 ... 3: 64) and first entry; at most three boxes since
+// round8(rank) <= 72.  A unit's b area holds the boxes in this order, box k at
+// byte j0[k] * 512 (256 rows of j0[k] entries before it).
+struct ExpBoxes {
+  int n, wi[3], j0[3];
+};
+__device__ __forceinline__ int widest(int v) { return v >= 64 ? 3 : v >= 32 ? 2 : v >= 16 ? 1 : 0; }
+__device__ __forceinline__ ExpBoxes exp_boxes(int r8) {
+  ExpBoxes b;
+  b.wi[0] = widest(r8);
+  b.j0[0] = 0;
+  const int r1 = r8 - (8 << b.wi[0]);
+  b.wi[1] = widest(r1);
+  b.j0[1] = 8 << b.wi[0];
+  const int r2 = r1 - (r1 > 0 ? 8 << b.wi[1] : 0);
+  b.wi[2] = widest(r2);
+  b.j0[2] = b.j0[1] + (8 << b.wi[1]);
+  b.n = r1 <= 0 ? 1 : r2 <= 0 ? 2 : 3;
+  return b;
+}
+// Byte offset of entries (j, j + 1) of row c in a unit's b area (j even, j < r8),
+// written as off + (c / 8) * stride: the swizzle of a row depends on c % 8 only.
+__device__ __forceinline__ void exp_boff(const ExpBoxes &bx, int c8, int j, int &off, int &stride) {
+  int wi = bx.wi[0], j0 = 0;
+  if (bx.n > 1 && j >= bx.j0[1]) {
+    wi = bx.wi[1];
+    j0 = bx.j0[1];
+  }
+  if (bx.n > 2 && j >= bx.j0[2]) {
+    wi = bx.wi[2];
+    j0 = bx.j0[2];
+  }
+  const int jj = j - j0, ch = jj >> 3;
+  // 16-byte chunk ch of a (16 << wi)-byte row, swizzled as the copy wrote it
+  const int sw = wi == 3 ? c8 : wi == 2 ? ((c8 >> 1) & 3) : wi == 1 ? ((c8 >> 2) & 1) : 0;
+  off = j0 * ECB * 2 + c8 * (16 << wi) + ((ch ^ sw) << 4) + (jj & 7) * 2;
+  stride = 8 * (16 << wi);
+}
+// The slice holding unit u of a tile, and its end.
+__device__ __forceinline__ int slice_of(const DecExpArgs &p, int u) {
+  int i = 0;
+  while (i + 1 < p.n && p.blk0[i + 1] <= u) ++i;
+  return i;
+}
+
+// Warp 0 loads, warps 1..8 compute, warp 9 stores the updated y rows.  Only
+// the loader walks the tile list (it runs stages ahead, so the latency of
+// those reads is hidden): before arming a stage it writes the stage's header
+// (tile, slice, columns, token rows, scale) and the tile's h rows of the slice
+// into shared memory, where the compute and store warps read them.
+constexpr int ECW = 8;                       // compute warps of the expand
+constexpr int ESW = ECW + 1;
+constexpr int NTHR_E = 32 * (ECW + 2);
+constexpr int EHR = 80;                      // h entries per token row in a header (round16(72))
+
+// h first: the compute warps read it as float2 pairs (8-byte aligned)
+struct __align__(16) ExpHdr {
+  float h[kDecTokens][EHR];   // zero past the rank and past the tile's tokens
+  int rows[kDecTokens];
+  int len, rank, r8, i, c0, nq, last;
+  float sc;
+};
+static_assert(offsetof(ExpHdr, h) == 0 && (EHR * 4) % 16 == 0, "header rows must stay 16-byte aligned");
+constexpr int kHdr = (int)((sizeof(ExpHdr) + 127) / 128 * 128);
+
+// KS: 16-entry steps of the rank at most (round16(R) / 16).
+template <int KS>
+__global__ void __launch_bounds__(NTHR_E, 1)
+    expand_dec_kernel(const __grid_constant__ DecExpMaps mp, DecExpArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *hdr_base = ring + kRing;
+  uint64_t *full = reinterpret_cast<uint64_t *>(hdr_base + NS * kHdr), *empty = full + NS, *ydone = empty + NS;
+  int64_t *s_run = reinterpret_cast<int64_t *>(ydone + NS);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&ydone[s], ECW);
+    }
+    fence_barrier_init();
+    s_run[0] = s_run[1] = 0;
+  }
+  __syncthreads();
+  pdl_wait();
+  // the cost split: a tile's unit weighs round8(rank) + 2 len + C0
+  const int ntiles = p.header[1];
+  Split sp;
+  sp.nk = p.nbu;
+  sp.n = 1;
+  sp.tw = 2;
+  sp.W = (int64_t)p.nbu * ((int64_t)p.header[2] + 2 * (int64_t)p.header[0] + (int64_t)C0 * ntiles);
+  sp.G = (int)gridDim.x;
+  const int cta = blockIdx.x;
+  const bool active = sp.W > 0;
+  if (active) {
+    const int64_t a0 = sp.begin(cta), a1 = sp.begin(cta + 1);
+    for (int t = threadIdx.x; t < ntiles; t += NTHR_E) {
+      const int4 td = p.tiles[t];
+      const int rn = t + 1 < ntiles ? p.tiles[t + 1].w : p.header[2];
+      const int64_t base = sp.base(t, td.y, td.w), w = (int64_t)(rn - td.w) + 2 * td.z + C0;
+      const int64_t end = base + (int64_t)p.nbu * w;
+      if (a0 >= base && a0 < end) s_run[0] = (int64_t)t * p.nbu + (a0 - base + w - 1) / w;
+      if (a1 >= base && a1 < end) s_run[1] = (int64_t)t * p.nbu + (a1 - base + w - 1) / w;
+    }
+    if (threadIdx.x == 0 && a1 >= sp.W) s_run[1] = (int64_t)ntiles * p.nbu;
+  }
+  __syncthreads();
+  const int64_t u0 = active ? s_run[0] : 0, u1 = active ? s_run[1] : 0;
+  const int nbu = p.nbu;
+  const bool any = u0 < u1;
+  const int64_t tb0 = any ? u0 / nbu : 0, tb1 = any ? (u1 - 1) / nbu : -1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ loader warp
+    int g = 0;
+    bool ok = true;
+    for (int64_t tile = tb0; ok && tile <= tb1; ++tile) {
+      const ExpTile t = exp_tile(p, (int)tile, ntiles);
+      const ExpBoxes bx = exp_boxes(t.r8);
+      const int bslot = p.b_one_slot ? 0 : t.slot;
+      const float sc = p.scal[t.slot];
+      int rows[kDecTokens];
+#pragma unroll
+      for (int e = 0; e < kDecTokens; ++e) rows[e] = e < t.len ? p.perm[t.start + e] : 0;
+      int kb, ke;
+      tile_chunks(tile, u0, u1, nbu, kb, ke);
+      int cur_i = -1;
+      float hv[kDecTokens * EHR / 32];   // this lane's h entries (e, j) = (idx / EHR, idx % EHR), idx = lane + 32 k
+      for (int u = kb; u < ke; ++g) {
+        const int i = slice_of(p, u), nq = min(min(t.q, ke - u), p.blk0[i + 1] - u), s = g % NS;
+        const int c0 = (u - p.blk0[i]) * ECB;
+        if (i != cur_i) {
+          cur_i = i;
+#pragma unroll
+          for (int k = 0; k < kDecTokens * EHR / 32; ++k) {
+            const int idx = lane + 32 * k, e = idx / EHR, j = idx - e * EHR;
+            int r = rows[0];
+#pragma unroll
+            for (int q = 1; q < kDecTokens; ++q)
+              if (e == q) r = rows[q];
+            hv[k] = e < t.len && j < t.rank ? p.h[(int64_t)r * p.ldh + (int64_t)i * p.R + j] : 0.f;
+          }
+        }
+        if (g >= NS && !(ok = wait_lane0(&empty[s], ((g / NS) & 1) ^ 1))) break;
+        // the stage's header, then the barrier that publishes it with the copies
+        ExpHdr *H = reinterpret_cast<ExpHdr *>(hdr_base + s * kHdr);
+#pragma unroll
+        for (int k = 0; k < kDecTokens * EHR / 32; ++k) {
+          const int idx = lane + 32 * k, e = idx / EHR, j = idx - e * EHR;
+          H->h[e][j] = hv[k];
+        }
+        if (lane == 0) {
+          H->len = t.len;
+          H->rank = t.rank;
+          H->r8 = t.r8;
+          H->i = i;
+          H->c0 = c0;
+          H->nq = nq;
+          H->last = tile == tb1 && u + nq >= ke;
+          H->sc = sc;
+#pragma unroll
+          for (int e = 0; e < kDecTokens; ++e) H->rows[e] = rows[e];
+        }
+        __syncwarp();
+        uint8_t *sy = ring + s * STAGE, *sb = sy + nq * EYA;
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(nq * (t.len * EYB + t.ng * EGB)));
+        __syncwarp();
+        const int per = t.len + bx.n;
+        for (int idx = lane; idx < nq * per; idx += 32) {
+          const int kq = idx / per, e = idx - kq * per, col = c0 + kq * ECB;
+          if (e < t.len) {
+            int r = rows[0];
+#pragma unroll
+            for (int k = 1; k < kDecTokens; ++k)
+              if (e == k) r = rows[k];
+            tma_load_2d(sy + (kq * kDecTokens + e) * EYB, &mp.y[i], &full[s], col, r);
+          } else {
+            const int k = e - t.len;
+            const int wi = k == 0 ? bx.wi[0] : k == 1 ? bx.wi[1] : bx.wi[2];
+            const int j0 = k == 0 ? 0 : k == 1 ? bx.j0[1] : bx.j0[2];
+            const CUtensorMap *m = wi == 3 ? &mp.b[i][3] : wi == 2 ? &mp.b[i][2] : wi == 1 ? &mp.b[i][1] : &mp.b[i][0];
+            tma_load_3d(sb + kq * t.ng * EGB + j0 * ECB * 2, m, &full[s], j0, col, bslot);
+          }
+        }
+        u += nq;
+      }
+    }
+  } else if (warp < ESW) {
+    // ------------------------------------------------------------------ compute warps
+    const int w = warp - 1;
+    const int gm = lane >> 2, gt = (lane & 3) << 1;   // fragment row (token) / column pair
+    int cur_r8 = -1, cur_rank = -1;
+    int boff[KS][2], bstr[KS][2];
+    uint32_t bmsk[KS][2];
+    for (int g = 0; any; ++g) {
+      const int s = g % NS;
+      if (!wait_lane0(&full[s], (g / NS) & 1)) break;
+      const ExpHdr *H = reinterpret_cast<const ExpHdr *>(hdr_base + s * kHdr);
+      const int len = H->len, rank = H->rank, r8 = H->r8, nq = H->nq, last = H->last;
+      const float sc = H->sc;
+      if (r8 != cur_r8 || rank != cur_rank) {
+        // this lane's B pieces: byte offset (8-column group 0), stride per
+        // 8-column group and rank mask of entries 16 ks + 8 hf + gt, gt + 1
+        cur_r8 = r8;
+        cur_rank = rank;
+        const ExpBoxes bx = exp_boxes(r8);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int j = 16 * ks + 8 * hf + gt;
+            boff[ks][hf] = 0;
+            bstr[ks][hf] = 0;
+            if (j < r8) exp_boff(bx, gm, j, boff[ks][hf], bstr[ks][hf]);
+            bmsk[ks][hf] = j >= rank ? 0u : j + 1 >= rank ? 0xffffu : 0xffffffffu;
+          }
+      }
+      // A fragments a0 / a2 of the tile's h rows: high part and residual
+      const int kst = (r8 + 15) / 16, ng = r8 / 8;
+      uint32_t ahi[KS][2], alo[KS][2];
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int j = 16 * ks + 8 * hf + gt;   // below 16 kst <= EHR when ks < kst
+          float2 v = make_float2(0.f, 0.f);
+          if (ks < kst && gm < kDecTokens) v = *reinterpret_cast<const float2 *>(&H->h[gm][j]);
+          const float v0 = v.x, v1 = v.y;
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
+          ahi[ks][hf] = pack_bf16(v0, v1);
+          alo[ks][hf] = pack_bf16(v0 - __bfloat162float(h0), v1 - __bfloat162float(h1));
+        }
+      uint8_t *sy = ring + s * STAGE;
+      const uint8_t *sb = sy + nq * EYA;
+      for (int kq = 0; kq < nq; ++kq) {
+        const uint8_t *bu = sb + kq * ng * EGB;
+#pragma unroll
+        for (int q = 0; q < ECB / 8 / ECW; ++q) {
+          const int nt = w + q * ECW;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            if (ks >= kst) break;
+            uint32_t b[2];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+              b[hf] = bmsk[ks][hf] ? *reinterpret_cast<const uint32_t *>(bu + boff[ks][hf] + nt * bstr[ks][hf]) &
+                                         bmsk[ks][hf]
+                                   : 0u;
+            const uint32_t ah[4] = {ahi[ks][0], 0u, ahi[ks][1], 0u}, al[4] = {alo[ks][0], 0u, alo[ks][1], 0u};
+            mma_bf16(acc, ah, b[0], b[1]);
+            mma_bf16(acc, al, b[0], b[1]);
+          }
+          if (gm < len) {
+            uint32_t *yp = reinterpret_cast<uint32_t *>(sy + (kq * kDecTokens + gm) * EYB + (8 * nt + gt) * 2);
+            const float2 y = unpack_bf16(*yp);
+            *yp = pack_bf16(y.x + sc * acc[0], y.y + sc * acc[1]);
+          }
+        }
+      }
+      // the store warp reads the updated rows through the async proxy
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ydone[s]);
+      if (last) break;
+    }
+  } else {
+    // ------------------------------------------------------------------ store warp
+    // stores stage g's rows once the compute warps are done with it (the copies
+    // dealt over the lanes; each lane waits for its own), and frees stage g - 1
+    // when its stores have read their shared memory (one group in flight)
+    int prev = -1;
+    for (int g = 0; any; ++g) {
+      const int s = g % NS;
+      if (!wait_lane0(&ydone[s], (g / NS) & 1)) break;
+      const ExpHdr *H = reinterpret_cast<const ExpHdr *>(hdr_base + s * kHdr);
+      const int len = H->len, i = H->i, c0 = H->c0, nq = H->nq, last = H->last;
+      const uint8_t *sy = ring + s * STAGE;
+      for (int idx = lane; idx < nq * len; idx += 32) {
+        const int kq = idx / len, e = idx - kq * len;
+        tma_store_2d(&mp.y[i], sy + (kq * kDecTokens + e) * EYB, c0 + kq * ECB, H->rows[e]);
+      }
+      bulk_commit();
+      bulk_wait_read1();
+      __syncwarp();
+      if (lane == 0 && prev >= 0) mbar_arrive(&empty[prev]);
+      prev = s;
+      if (last) break;
+    }
+    bulk_wait_read_all();
+    __syncwarp();
+    if (lane == 0 && prev >= 0) mbar_arrive(&empty[prev]);
+    bulk_wait_all();
+  }
+  pdl_launch_dependents();
+}
+
+template <int KS>
+lora_status_t exp_launch(const DecExpMaps &mp, const DecExpArgs &p, cudaStream_t st) {
+  const size_t smem = 1024 + kRing + NS * kHdr + 256;
+  LORA_CUDA(ensure_smem((const void *)expand_dec_kernel<KS>, smem));
+  const int occ = occupancy((const void *)expand_dec_kernel<KS>, NTHR_E, smem);
+  const int G = std::max(1, std::min(occ * num_sms(), kMaxDecGrid));
+  LORA_CUDA(launch(expand_dec_kernel<KS>, dim3((unsigned)G), dim3(NTHR_E), smem, st, 1, true, mp, p));
+  return LORA_OK;
+}
+
 int read_clear_error() {
   int v = 0, z = 0;
   if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return -1;
@@ -407,6 +756,62 @@ lora_status_t shrink_dec_launch(const DecArgs &args, const MultiArgs &m, int64_t
   if (blocks <= 1) return launch_rbk<1>(tmX, tmA, p, st);
   if (blocks <= 2) return launch_rbk<2>(tmX, tmA, p, st);
   if (blocks <= 4) return launch_rbk<4>(tmX, tmA, p, st);
+  return LORA_ERR_UNSUPPORTED;
+}
+
+lora_status_t expand_dec_launch(const DecExpArgs &args, const MultiArgs &m, int64_t T, cudaStream_t st) {
+  using namespace dec;
+  DecExpArgs p = args;
+  DecExpMaps mp;
+  memset(&mp, 0, sizeof(mp));
+  const int R = m.addr.max_rank;
+  // one unit (y rows and round8(R) / 8 boxes of b) must fit a stage
+  if (EYA + ceil_div(round_up(R, 8), 8) * EGB > STAGE) return LORA_ERR_UNSUPPORTED;
+  p.b_one_slot = m.sb_slot == 0 ? 1 : 0;
+  int off = 0, nb = 0;
+  for (int i = 0; i < m.n; ++i) {
+    const int64_t w = m.out_slices[i];
+    p.blk0[i] = nb;
+    nb += (int)ceil_div(w, ECB);
+    {
+      // y columns of slice i: one 256-column row segment per copy
+      uint64_t dims[2] = {(uint64_t)w, (uint64_t)T};
+      uint64_t str[1] = {(uint64_t)m.ldy * 2};
+      uint32_t box[2] = {ECB, 1};
+      if (!encode_tmap(&mp.y[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (const __nv_bfloat16 *)m.y + off, dims, str,
+                       box, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return LORA_ERR_ALIGNMENT;
+    }
+    // b rows of slice i: boxes of 8, 16, 32 or 64 rank entries x 256 rows (the
+    // wider ones swizzled over their 32-, 64- or 128-byte rows), no sector promotion
+    const int64_t bS = p.b_one_slot ? 1 : m.addr.num_slots;
+    const int64_t sslot = p.b_one_slot ? m.O * m.sb_row : m.sb_slot;
+    const CUtensorMapSwizzle swz[4] = {CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                                       CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_SWIZZLE_128B};
+    for (int wi = 0; wi < 4 && (8 << wi) <= round_up(R, 8); ++wi) {
+      uint64_t dims[3] = {(uint64_t)R, (uint64_t)w, (uint64_t)bS};
+      uint64_t str[2] = {(uint64_t)m.sb_row * 2, (uint64_t)sslot * 2};
+      uint32_t box[3] = {(uint32_t)(8 << wi), ECB, 1};
+      if (!encode_tmap(&mp.b[i][wi], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                       (const __nv_bfloat16 *)m.b + (int64_t)off * m.sb_row, dims, str, box, swz[wi],
+                       CU_TENSOR_MAP_L2_PROMOTION_NONE))
+        return LORA_ERR_ALIGNMENT;
+    }
+    off += (int)w;
+  }
+  p.blk0[m.n] = nb;
+  p.nbu = nb;
+  // bytes HBM serves per b row: the row itself when rows are at most 128 bytes
+  // (neighbouring rows share the lines), else whole 128-byte lines; for the
+  // 256 rows of a unit, in 512-byte units
+  const int64_t r8b = round_up(R, 8) * 2, rowb = r8b <= 128 ? r8b : round_up(r8b, 128);
+  p.bw = (int)(ECB * rowb / 512);
+  if (nb == 0) return LORA_OK;
+  const int ks = (int)ceil_div(round_up(R, 8), 16);
+  if (ks <= 1) return exp_launch<1>(mp, p, st);
+  if (ks <= 2) return exp_launch<2>(mp, p, st);
+  if (ks <= 4) return exp_launch<4>(mp, p, st);
+  if (ks <= 8) return exp_launch<8>(mp, p, st);
   return LORA_ERR_UNSUPPORTED;
 }
 

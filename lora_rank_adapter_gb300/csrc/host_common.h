@@ -36,8 +36,11 @@ inline int rank_bucket(int r) { return r <= 16 ? 16 : r <= 32 ? 32 : r <= 64 ? 6
 // Encodes a 2-D/3-D bf16 or fp32 tiled tensor map.  dims/strides in elements
 // (strides of dims 1.. in elements of the innermost type).  Returns false if
 // the driver rejects it.
+// `promo` is the L2 sector promotion of the copies (256-byte lines for dense
+// streams; none for strided reads that use a few bytes of each row).
 bool encode_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base, const uint64_t *dims,
-                 const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swz);
+                 const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swz,
+                 CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 
 // SM count of the current device, and resident blocks per SM of a kernel
 // (both cached per device).

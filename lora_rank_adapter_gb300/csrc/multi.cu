@@ -1307,12 +1307,35 @@ lora_status_t shrink(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t st) {
   return schedule_then_shrink(m, c, sp, st);
 }
 
+// The expand of a scheduled batch: decode batches stream b through TMA on the
+// persistent decode kernel (the plain-load kernel when y or b cannot be read
+// through tensor maps, or R > 72); prefill batches run the tiled expand.
+lora_status_t expand_scheduled(const MultiArgs &m, const SchedPtrs &sp, cudaStream_t st) {
+  if (decode_shape(m.addr.num_tokens, m.addr.num_slots)) {
+    DecExpArgs a{};
+    a.ranks = m.ranks;
+    a.scal = m.scalings;
+    a.header = sp.header;
+    a.tiles = sp.tiles;
+    a.perm = sp.perm;
+    a.S = m.addr.num_slots;
+    a.R = m.addr.max_rank;
+    a.n = m.n;
+    a.T = m.addr.num_tokens;
+    a.h = m.h;
+    a.ldh = m.ldh;
+    const lora_status_t r = expand_dec_launch(a, m, m.addr.num_tokens, st);
+    if (r != LORA_ERR_ALIGNMENT && r != LORA_ERR_UNSUPPORTED) return r;
+  }
+  return dispatch_expand(margs(m, sp), m.addr.num_tokens, st);
+}
+
 lora_status_t expand(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t st) {
   LORA_TRY(check_seg(m, false, true));
   WsCarver c(ws, ws_bytes);
   SchedPtrs sp;
   LORA_TRY(schedule(m, c, sp, st));
-  return dispatch_expand(margs(m, sp), m.addr.num_tokens, st);
+  return expand_scheduled(m, sp, st);
 }
 
 lora_status_t apply_linear(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t st) {
@@ -1324,7 +1347,7 @@ lora_status_t apply_linear(MultiArgs m, void *ws, size_t ws_bytes, cudaStream_t 
   m.h = h;
   m.ldh = (int64_t)m.n * m.addr.max_rank;
   LORA_TRY(schedule_then_shrink(m, c, sp, st));
-  return dispatch_expand(margs(m, sp), m.addr.num_tokens, st);
+  return expand_scheduled(m, sp, st);
 }
 
 lora_status_t gather_shrink(MultiArgs m, cudaStream_t st) {
