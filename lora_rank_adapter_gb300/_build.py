@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIB_DIR, "liblora.so")
-SOURCES = ["api.cu", "single_bf16.cu", "single_tc.cu", "single_f32.cu", "multi.cu", "decode.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "single_common.cu", "single_tc.cu", "single_f32.cu", "multi.cu", "decode.cu", "noalloc.cu"]
 ARCH = "arch=compute_103a,code=sm_103a"
 NVCC_FLAGS = ["-std=c++17", "-O3", "-gencode", ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden"]

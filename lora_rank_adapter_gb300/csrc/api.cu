@@ -12,7 +12,7 @@
 
 #include "host_common.h"
 #include "multi.h"
-#include "single_bf16.h"
+#include "single_common.h"
 #include "single_tc.h"
 #include "decode.h"
 
@@ -454,7 +454,7 @@ lora_status_t lora_gather_shrink(const lora_addressing_t *addr, const int32_t *r
 lora_status_t lora_device_error(int32_t *code) {
   if (code == nullptr) return LORA_ERR_INVALID_ARG;
   int v = 0;
-  int parts[5] = {read_clear_error_single_bf16(), read_clear_error_single_f32(), read_clear_error_multi(),
+  int parts[5] = {read_clear_error_single_common(), read_clear_error_single_f32(), read_clear_error_multi(),
                   read_clear_error_single_tc(), read_clear_error_decode()};
   for (int p : parts) {
     if (p < 0) return LORA_ERR_CUDA;

@@ -1,4 +1,4 @@
-// single_bf16.h -- argument structs and launchers shared by the single-adapter
+// single_common.h -- argument structs and helpers shared by the single-adapter
 // kernels and the C ABI layer.
 #pragma once
 
@@ -36,43 +36,8 @@ struct SingleLayout {
   int64_t lda = 0, ldb = 0;
 };
 
-struct FwdArgs {
-  int M, K, L;
-  float scale;
-  int cl;
-  float *h;        // optional: h = X * A, [M][ldh] fp32, columns j < r
-  int64_t ldh;
-  int r;
-};
-
-struct RowsArgs {
-  int M, Kc, csplit;
-  uint8_t *blob;     // [ceil(M/64)] x (hi, lo) bf16 [64][RP] tiles
-  int *counters;
-  int ncounters;
-};
-
-struct ColArgs {
-  int M, K, r, msplit, nkb;   // for dB, K holds L and nkb the number of 64-column blocks of L
-  float scale;
-  float *part_out;
-  int *counters;
-  float *out;                 // bf16 elements when out_bf16
-  int64_t out_s0, out_s1;
-  int out_bf16;
-  const uint8_t *blob;        // the row pass's hi/lo tiles of dyb (dX/dA) or h (dB)
-  const __nv_bfloat16 *dx_old;   // dX pass: dX to add to (nullptr: overwrite)
-  int64_t lddx;
-};
-
 SingleLayout plan_layout(const SingleArgs &a, bool need_A, bool need_B);
-size_t bf16_ws_bytes(int op, int64_t M, int64_t K, int64_t L, int r);
 size_t f32_ws_bytes(int op, int64_t M, int64_t K, int64_t L, int r);
-
-lora_status_t forward_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
-lora_status_t backward_dx_da_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
-lora_status_t backward_db_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
-lora_status_t backward_bf16(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
 
 lora_status_t forward_f32(const SingleArgs &a, cudaStream_t st);
 lora_status_t backward_dx_da_f32(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
@@ -87,7 +52,7 @@ lora_status_t pack_bf16_2d(const void *src, int64_t s_row, int64_t s_col, int64_
 lora_status_t fill_zero_2d(lora_dtype_t dt, void *p, int64_t rows, int64_t cols, int64_t s_row, int64_t s_col,
                            cudaStream_t st);
 
-int read_clear_error_single_bf16();
+int read_clear_error_single_common();
 int read_clear_error_single_f32();
 
 }  // namespace lora

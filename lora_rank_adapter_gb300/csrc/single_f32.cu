@@ -9,7 +9,7 @@
 
 #include "common.cuh"
 #include "host_common.h"
-#include "single_bf16.h"
+#include "single_common.h"
 
 namespace lora {
 

@@ -43,7 +43,7 @@
 
 #include "common.cuh"
 #include "host_common.h"
-#include "single_bf16.h"
+#include "single_common.h"
 #include "single_tc.h"
 #include "tc_common.cuh"
 

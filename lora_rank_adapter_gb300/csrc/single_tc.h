@@ -7,7 +7,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "single_bf16.h"
+#include "single_common.h"
 
 namespace lora {
 
