@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
                                                      int4 *tiles, int bmt, int *zero, int nzero) {
   extern __shared__ int gsm[];
   const int nw = blockDim.x >> 5;
-  int *hist = gsm;                 // [nw][S]
+  int *hist = gsm;                 // [S][nw]: a slot's warp counts contiguous
   int *srank = gsm + nw * S;       // [S]
   int *scnt = srank + S;           // [S] active tokens of each slot
   int *sbase = scnt + S;           // [S] first position of each slot in the permutation
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
       // inactive lanes share one class (fewer distinct values: a faster match)
       const bool act = active(sv[u]);
       const unsigned m = same_key_lanes(act ? sv[u] : -1);
-      if (act && (m & lt) == 0) hist[warp * S + sv[u]] += __popc(m);
+      if (act && (m & lt) == 0) hist[sv[u] * nw + warp] += __popc(m);
       __syncwarp();
     }
   }
@@ -234,14 +234,14 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
   // per slot, a warp scans the warps' counts (lane w: warp w): hist becomes each
   // warp's offset inside the slot, scnt the slot's total
   for (int s = warp; s < S; s += nw) {
-    const int v = lane < nw ? hist[lane * S + s] : 0;
+    const int v = lane < nw ? hist[s * nw + lane] : 0;
     int inc = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int n = __shfl_up_sync(0xffffffffu, inc, o);
       if (lane >= o) inc += n;
     }
-    if (lane < nw) hist[lane * S + s] = inc - v;
+    if (lane < nw) hist[s * nw + lane] = inc - v;
     if (lane == 31) scnt[s] = inc;
   }
   __syncthreads();
@@ -289,11 +289,11 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
       const bool act = active(sv[u]);
       const unsigned m = same_key_lanes(act ? sv[u] : -1);
       int cur = 0;
-      if (act) cur = sbase[sv[u]] + hist[warp * S + sv[u]];
+      if (act) cur = sbase[sv[u]] + hist[sv[u] * nw + warp];
       __syncwarp();
       if (act) {
         perm_out[cur + __popc(m & lt)] = t;
-        if ((m & lt) == 0) hist[warp * S + sv[u]] = cur - sbase[sv[u]] + __popc(m);
+        if ((m & lt) == 0) hist[sv[u] * nw + warp] = cur - sbase[sv[u]] + __popc(m);
       }
       __syncwarp();
     }
