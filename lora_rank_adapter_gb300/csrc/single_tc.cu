@@ -286,11 +286,14 @@ struct ExpCfg {
   static constexpr int B_B = BOXC * RP * 2;      // B^T chunk [64 l][RP]
   static constexpr int STAGE = Y_B + B_B;
   static constexpr int HB = 2 * blob_tile(RP);   // hi + lo of one row block
-  static constexpr int NS0 = (kRingBytes - 2 * HB) / STAGE;
+  // blob buffers: a row block covers L / 64 chunks, so at r = 64 one buffer
+  // (a short stall when the row block changes) buys the ring another stage
+  static constexpr int NB = RP >= 64 ? 1 : 2;
+  static constexpr int NS0 = (kRingBytes - NB * HB) / STAGE;
   static constexpr int NS = NS0 > 8 ? 8 : NS0;
   static constexpr int ND = 4;
   static constexpr int TMEM = 256;
-  static constexpr int BYTES = 1024 + 2 * HB + NS * STAGE + 1024;
+  static constexpr int BYTES = 1024 + NB * HB + NS * STAGE + 1024;
 };
 
 template <int RP>
@@ -298,10 +301,10 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
                                                          const __grid_constant__ CUtensorMap tmYs,
                                                          const __grid_constant__ CUtensorMap tmB, TcExpArgs p) {
   using C = ExpCfg<RP>;
-  constexpr int NS = C::NS, PW = C::PW, ND = C::ND;
+  constexpr int NS = C::NS, PW = C::PW, ND = C::ND, NB = C::NB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *hbuf = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *ring = hbuf + 2 * C::HB;
+  uint8_t *ring = hbuf + NB * C::HB;
   uint64_t *full = reinterpret_cast<uint64_t *>(ring + NS * C::STAGE);
   uint64_t *empty = full + NS;
   uint64_t *hfull = empty + NS;    // [2]
@@ -346,14 +349,6 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
       for (int64_t u = u0; u < u1; ++u) {
         const int64_t rb = u / nl;
         const int lc = (int)(u % nl);
-        if (rb != prev) {
-          const int hb = hidx & 1;
-          if (hidx >= 2 && !mbar_wait(&hempty[hb], ((hidx >> 1) & 1) ^ 1)) break;
-          mbar_arrive_expect_tx(&hfull[hb], C::HB);
-          bulk_load(hbuf + hb * C::HB, p.blob + rb * (int64_t)C::HB, C::HB, &hfull[hb]);
-          prev = rb;
-          ++hidx;
-        }
         const int g = (int)(u - u0), s = g % NS;
         if (g >= NS && !mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) break;
         uint8_t *st = ring + s * C::STAGE;
@@ -362,6 +357,16 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
 #pragma unroll
         for (int pp = 0; pp < RP / PW; ++pp)
           tma_load_2d(st + C::Y_B + pp * (BOXC * PW * 2), &tmB, &full[s], pp * PW, lc * BOXC);
+        // the row block's blob after the unit's stage (which does not need it), so
+        // that a buffer still read by the previous block's MMAs delays no Y copy
+        if (rb != prev) {
+          const int hb = hidx % NB;
+          if (hidx >= NB && !mbar_wait(&hempty[hb], ((hidx / NB) & 1) ^ 1)) break;
+          mbar_arrive_expect_tx(&hfull[hb], C::HB);
+          bulk_load(hbuf + hb * C::HB, p.blob + rb * (int64_t)C::HB, C::HB, &hfull[hb]);
+          prev = rb;
+          ++hidx;
+        }
       }
     }
   } else if (warp == 1) {
@@ -373,8 +378,8 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
       for (int64_t u = u0; ok && u < u1; ++u) {
         const int64_t rb = u / nl;
         if (rb != prev) {
-          hb = hidx & 1;
-          if (!(ok = mbar_wait(&hfull[hb], (hidx >> 1) & 1))) break;
+          hb = hidx % NB;
+          if (!(ok = mbar_wait(&hfull[hb], (hidx / NB) & 1))) break;
           prev = rb;
           ++hidx;
         }
@@ -782,12 +787,10 @@ bool map_bc_tc(CUtensorMap *m, const void *p, int64_t L, int r, int64_t ldb, int
 }
 
 // Persistent grid: every SM holds one CTA of these kernels (their shared memory
-// allows no more), at most one CTA per unit.
-int grid_for(int64_t units, const void *kern, size_t smem);
-
-// Stream-K passes give every CTA at least kMinUnits units (fewer CTAs on small
-// problems, and a bound on the partial sums), at most kMaxGrid CTAs (one per SM;
-// more than any GB300 has), so that workspace sizes depend on the arguments only.
+// allows no more).  Stream-K passes give every CTA at least min_units units
+// (kMinUnits: fewer CTAs on small problems, and a bound on the partial sums), at
+// most kMaxGrid CTAs (one per SM; more than any GB300 has), so that workspace
+// sizes depend on the arguments only.
 constexpr int kMinUnits = 8;
 constexpr int kMaxGrid = 160;
 int grid_for(int64_t units, const void *kern, size_t smem, int min_units) {
