@@ -499,6 +499,8 @@ __global__ void __launch_bounds__(NTHR_E, 1)
       if (a0 >= base && a0 < end) s_run[0] = (int64_t)t * p.nbu + (a0 - base + w - 1) / w;
       if (a1 >= base && a1 < end) s_run[1] = (int64_t)t * p.nbu + (a1 - base + w - 1) / w;
     }
+    // the whole grid takes part, so with W < G the last runs begin at W: empty
+    if (threadIdx.x == 0 && a0 >= sp.W) s_run[0] = (int64_t)ntiles * p.nbu;
     if (threadIdx.x == 0 && a1 >= sp.W) s_run[1] = (int64_t)ntiles * p.nbu;
   }
   __syncthreads();

@@ -239,6 +239,31 @@ def test_repeatable_bitwise_multi():
     assert torch.equal(outs[0], outs[1])
 
 
+@pytest.mark.parametrize("T,S,R,osl", [(1, 1, 8, [64]), (2, 2, 16, [24]), (5, 3, 16, [256, 40]), (9, 9, 64, [512])])
+def test_expand_tiny_batches_each_unit_once(T, S, R, osl):
+    """Decode batches whose split cost is below the grid size: with y0 = 0 a unit
+    that two CTAs both add into shows as a doubled delta.  Whether two such
+    read-modify-writes interleave depends on timing, so the expand runs many
+    times; every run must give the oracle's y, bit-identical to the first."""
+    w = workload(T, 64, osl, S, R, [R], "uniform", seed=T + 40, zero_y=True)
+    n = len(osl)
+    o = oracle_inputs(w)
+    href = O.shrink(o["x"], o["a"], o["slots"], o["ranks"], R, n)
+    h = torch.from_numpy(href.astype(np.float32)).to(DEV)
+    ref = O.expand(href.astype(np.float32).astype(np.float64), o["b"], o["slots"], o["ranks"], o["scal"],
+                   o["y0"], osl, R)
+    outs = []
+    for _ in range(40):
+        y = torch.zeros_like(w["y0"])
+        lora.lora_expand(h, w["b"], w["slots"], w["ranks"], w["scalings"], y, osl, R)
+        outs.append(y)
+    torch.cuda.synchronize()
+    assert lora.lora_device_error() == 0
+    assert rel_err(f64(outs[0]), ref) <= TOL_BF16
+    for y in outs[1:]:
+        assert torch.equal(y, outs[0])
+
+
 def test_c4_prefill_full():
     """The prefill workload at full size: T = 4096, fused QKV [4096, 1024, 1024]."""
     spec = synth.multi_spec("multi_c4")
