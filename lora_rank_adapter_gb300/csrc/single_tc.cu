@@ -284,16 +284,22 @@ struct ExpCfg {
   static constexpr int PW = pw_of(RP);
   static constexpr int Y_B = TM * BOXC * 2;      // 16 KB
   static constexpr int B_B = BOXC * RP * 2;      // B^T chunk [64 l][RP]
-  static constexpr int STAGE = Y_B + B_B;
   static constexpr int HB = 2 * blob_tile(RP);   // hi + lo of one row block
   // blob buffers: a row block covers L / 64 chunks, so at r = 64 one buffer
-  // (a short stall when the row block changes) buys the ring another stage
+  // (a short stall when the row block changes) buys the ring more Y stages
   static constexpr int NB = RP >= 64 ? 1 : 2;
-  static constexpr int NS0 = (kRingBytes - NB * HB) / STAGE;
-  static constexpr int NS = NS0 > 8 ? 8 : NS0;
+  // Y tiles and B^T chunks have rings of their own: a Y stage is held until its
+  // tile has been stored, a B^T stage only until the MMAs have read it, and the
+  // MMAs never wait for a Y tile.  The loader issues both in unit order, so it
+  // runs at most NBB + ND units ahead of the epilogue: NBB = NS - ND lets the Y
+  // ring fill.
   static constexpr int ND = 4;
+  static constexpr int NS0 = (kRingBytes + 28 * 1024 - NB * HB + ND * B_B) / (Y_B + B_B);
+  static constexpr int NS = NS0 > 12 ? 12 : NS0;
+  static constexpr int NBB = NS - ND > 2 ? NS - ND : 2;
   static constexpr int TMEM = 256;
-  static constexpr int BYTES = 1024 + NB * HB + NS * STAGE + 1024;
+  static constexpr int BYTES = 1024 + NB * HB + NS * Y_B + NBB * B_B + 1024;
+  static_assert(BYTES <= 227 * 1024, "expand shared memory");
 };
 
 template <int RP>
@@ -301,13 +307,16 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
                                                          const __grid_constant__ CUtensorMap tmYs,
                                                          const __grid_constant__ CUtensorMap tmB, TcExpArgs p) {
   using C = ExpCfg<RP>;
-  constexpr int NS = C::NS, PW = C::PW, ND = C::ND, NB = C::NB;
+  constexpr int NS = C::NS, PW = C::PW, ND = C::ND, NB = C::NB, NBB = C::NBB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *hbuf = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *ring = hbuf + NB * C::HB;
-  uint64_t *full = reinterpret_cast<uint64_t *>(ring + NS * C::STAGE);
+  uint8_t *ring = hbuf + NB * C::HB;     // Y tiles
+  uint8_t *bring = ring + NS * C::Y_B;   // B^T chunks
+  uint64_t *full = reinterpret_cast<uint64_t *>(bring + NBB * C::B_B);
   uint64_t *empty = full + NS;
-  uint64_t *hfull = empty + NS;    // [2]
+  uint64_t *bfull = empty + NS;    // [NBB]
+  uint64_t *bempty = bfull + NBB;
+  uint64_t *hfull = bempty + NBB;  // [2]
   uint64_t *hempty = hfull + 2;    // [2]
   uint64_t *dfull = hempty + 2;    // [ND]
   uint64_t *dempty = dfull + ND;   // [ND]
@@ -321,6 +330,10 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 4);
+    }
+    for (int s = 0; s < NBB; ++s) {
+      mbar_init(&bfull[s], 1);
+      mbar_init(&bempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&hfull[b], 1);
@@ -349,14 +362,16 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
       for (int64_t u = u0; u < u1; ++u) {
         const int64_t rb = u / nl;
         const int lc = (int)(u % nl);
-        const int g = (int)(u - u0), s = g % NS;
+        const int g = (int)(u - u0), s = g % NS, sb = g % NBB;
         if (g >= NS && !mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) break;
-        uint8_t *st = ring + s * C::STAGE;
-        mbar_arrive_expect_tx(&full[s], C::STAGE);
-        tma_load_2d(st, &tmY, &full[s], lc * BOXC, (int)(rb * TM));
+        mbar_arrive_expect_tx(&full[s], C::Y_B);
+        tma_load_2d(ring + s * C::Y_B, &tmY, &full[s], lc * BOXC, (int)(rb * TM));
+        if (g >= NBB && !mbar_wait(&bempty[sb], ((g / NBB) & 1) ^ 1)) break;
+        uint8_t *bt = bring + sb * C::B_B;
+        mbar_arrive_expect_tx(&bfull[sb], C::B_B);
 #pragma unroll
         for (int pp = 0; pp < RP / PW; ++pp)
-          tma_load_2d(st + C::Y_B + pp * (BOXC * PW * 2), &tmB, &full[s], pp * PW, lc * BOXC);
+          tma_load_2d(bt + pp * (BOXC * PW * 2), &tmB, &bfull[sb], pp * PW, lc * BOXC);
         // the row block's blob after the unit's stage (which does not need it), so
         // that a buffer still read by the previous block's MMAs delays no Y copy
         if (rb != prev) {
@@ -383,11 +398,11 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
           prev = rb;
           ++hidx;
         }
-        const int g = (int)(u - u0), s = g % NS, b = g % ND;
+        const int g = (int)(u - u0), sb = g % NBB, b = g % ND;
         if (g >= ND && !(ok = mbar_wait(&dempty[b], ((g / ND) & 1) ^ 1))) break;
-        if (!(ok = mbar_wait(&full[s], (g / NS) & 1))) break;
+        if (!(ok = mbar_wait(&bfull[sb], (g / NBB) & 1))) break;
         tc_fence_after();
-        const uint32_t hh = smem_u32(hbuf + hb * C::HB), bb = smem_u32(ring + s * C::STAGE) + C::Y_B;
+        const uint32_t hh = smem_u32(hbuf + hb * C::HB), bb = smem_u32(bring + sb * C::B_B);
 #pragma unroll
         for (int part = 0; part < 2; ++part)
 #pragma unroll
@@ -398,6 +413,7 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
             tc_mma_bf16(tmem + b * BOXC, ad, bd, idesc, (part == 0 && qk == 0) ? 0u : 1u);
           }
         tc_commit(&dfull[b]);
+        tc_commit(&bempty[sb]);
         if (u == u1 - 1 || (u + 1) / nl != rb) tc_commit(&hempty[hb]);
       }
       tc_commit(mdone);
@@ -423,7 +439,7 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
       tmem_ld32(tl + b * BOXC, acc);
       tmem_ld32(tl + b * BOXC + 32, acc + 32);
       tc_fence_before();
-      uint8_t *yt = ring + s * C::STAGE;
+      uint8_t *yt = ring + s * C::Y_B;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint4 *yp = reinterpret_cast<uint4 *>(yt + swz(row, c * 16, 128));
@@ -472,13 +488,25 @@ struct ColCfg {
   static constexpr int PW = pw_of(RP);
   static constexpr int IN_B = 2 * TM * BOXC * 2;   // two 64-column boxes: 32 KB
   static constexpr int BL_B = 2 * blob_tile(RP);   // hi + lo
-  static constexpr int STAGE = IN_B + BL_B;
   static constexpr int AC_B = kDX ? 2 * RP * 128 : 0;   // A^T for dX: two [RP][64] boxes
-  static constexpr int NS0 = (kRingBytes + 28 * 1024 - AC_B) / STAGE;
-  static constexpr int NS = NS0 > 6 ? 6 : NS0;
-  static constexpr int TMEM = tmem_cols(2 * RP + (kDX ? 2 * TM : 0));
+  static constexpr int SPACE = kRingBytes + 28 * 1024 - AC_B;
+  // In tiles and blobs have rings of their own.  With dX an In stage is held
+  // until the dX tile written over it has been stored, a blob stage only until
+  // the MMAs have read it: two blob stages, the rest of the space In stages.
+  // Without dX both are released by the MMAs: as many blob stages as In stages.
+  static constexpr int NX0 = kDX ? (SPACE - 2 * BL_B) / IN_B : SPACE / (IN_B + BL_B);
+  static constexpr int NX = NX0 > 6 ? 6 : NX0;
+  static constexpr int NBL = kDX ? 2 : NX;
+  // The blob's hi and lo tiles lie one after the other, as two column panels of
+  // one [128][2 RP] operand: at RP <= 64 one MMA of N = 2 RP takes both (half
+  // the MMA issues; the accumulator's two halves are added when read out)
+  static constexpr bool HL = RP <= 64;
+  static constexpr int AW = HL ? 2 * RP : RP;      // TMEM columns of one accumulator
+  static constexpr int TMEM = tmem_cols(2 * AW + (kDX ? 2 * TM : 0));
   static constexpr int ACC0 = kDX ? 2 * TM : 0;   // first TMEM column of the accumulators
-  static constexpr int BYTES = 1024 + NS * STAGE + AC_B + 1024;
+  static constexpr int BYTES = 1024 + NX * IN_B + NBL * BL_B + AC_B + 1024;
+  static_assert(BYTES <= 227 * 1024, "column pass shared memory");
+  static_assert(2 * AW + (kDX ? 2 * TM : 0) <= 512, "column pass tensor memory");
 };
 
 template <int RP, bool kDX, bool kAccX>
@@ -486,13 +514,16 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
                                                       const __grid_constant__ CUtensorMap tmAc,
                                                       const __grid_constant__ CUtensorMap tmDX, TcColArgs p) {
   using C = ColCfg<RP, kDX>;
-  constexpr int NS = C::NS, PW = C::PW;
+  constexpr int NS = C::NX, NBL = C::NBL, PW = C::PW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *acbuf = ring + NS * C::STAGE;
+  uint8_t *bring = ring + NS * C::IN_B;   // blob stages
+  uint8_t *acbuf = bring + NBL * C::BL_B;
   uint64_t *full = reinterpret_cast<uint64_t *>(acbuf + C::AC_B);
   uint64_t *empty = full + NS;
-  uint64_t *afull = empty + NS;    // [2] accumulators
+  uint64_t *bfull = empty + NS;    // [NBL] blob stages
+  uint64_t *bempty = bfull + NBL;
+  uint64_t *afull = bempty + NBL;  // [2] accumulators
   uint64_t *aempty = afull + 2;
   uint64_t *dfull = aempty + 2;    // [2] dX tiles
   uint64_t *dempty = dfull + 2;
@@ -514,6 +545,10 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kDX ? 4 : 1);
       mbar_init(&xfree[s], 1);
+    }
+    for (int s = 0; s < NBL; ++s) {
+      mbar_init(&bfull[s], 1);
+      mbar_init(&bempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&afull[b], 1);
@@ -550,23 +585,25 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
           tma_load_2d(acbuf + RP * 128, &tmAc, acfull, cb * 2 * BOXC + BOXC, 0);
           ++seg;
         }
-        const int g = (int)(u - u0), s = g % NS;
+        const int g = (int)(u - u0), s = g % NS, sb = g % NBL;
         if (g >= NS && !mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) break;
-        uint8_t *st = ring + s * C::STAGE;
-        mbar_arrive_expect_tx(&full[s], C::STAGE);
+        uint8_t *st = ring + s * C::IN_B;
+        mbar_arrive_expect_tx(&full[s], C::IN_B);
         tma_load_2d(st, &tmIn, &full[s], cb * 2 * BOXC, t * TM);
         tma_load_2d(st + TM * BOXC * 2, &tmIn, &full[s], cb * 2 * BOXC + BOXC, t * TM);
-        bulk_load(st + C::IN_B, p.blob + (int64_t)t * C::BL_B, C::BL_B, &full[s]);
+        if (g >= NBL && !mbar_wait(&bempty[sb], ((g / NBL) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(&bfull[sb], C::BL_B);
+        bulk_load(bring + sb * C::BL_B, p.blob + (int64_t)t * C::BL_B, C::BL_B, &bfull[sb]);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t id_acc = tc_idesc(TM, RP, true, true);
+      const uint32_t id_acc = tc_idesc(TM, C::AW, true, true);
       const uint32_t id_dx = tc_idesc(TM, 2 * BOXC, false, true);
       int seg = 0;
       bool ok = true;
       for (int64_t u = u0; ok && u < u1; ++u) {
-        const int g = (int)(u - u0), s = g % NS;
+        const int g = (int)(u - u0), s = g % NS, sb = g % NBL;
         const int t = (int)(u % nt);
         const bool first = u == u0 || t == 0, last = u == u1 - 1 || t == nt - 1;
         const int ab = seg & 1;
@@ -575,10 +612,11 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
           if (kDX && !(ok = mbar_wait(acfull, seg & 1))) break;
         }
         if (!(ok = mbar_wait(&full[s], (g / NS) & 1))) break;
+        if (!(ok = mbar_wait(&bfull[sb], (g / NBL) & 1))) break;
         const int db = g & 1;
         if (kDX && g >= 2 && !(ok = mbar_wait(&dempty[db], ((g >> 1) & 1) ^ 1))) break;
         tc_fence_after();
-        const uint32_t st = smem_u32(ring + s * C::STAGE), bl = st + C::IN_B;
+        const uint32_t st = smem_u32(ring + s * C::IN_B), bl = smem_u32(bring + sb * C::BL_B);
         if (kDX) {
           // dX tile [128 rows][128 columns] = (dyb_hi + dyb_lo) * A^T
           const uint32_t ac = smem_u32(acbuf);
@@ -595,15 +633,17 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
           tc_commit(&dfull[db]);
         }
         // acc[c][j] += sum over the tile's 128 rows of In[row][c] * blob[row][j]
+        // (with HL: acc[c][j] from hi, acc[c][RP + j] from lo, in the same MMAs)
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
+        for (int part = 0; part < (C::HL ? 1 : 2); ++part)
 #pragma unroll
           for (int kk = 0; kk < TM / 16; ++kk) {
             const uint64_t ad = tc_desc(st + kk * 2048, TM * BOXC * 2, 1024, 128);
-            const uint64_t bd =
-                tc_desc(bl + part * blob_tile(RP) + kk * 16 * PW * 2, RP > PW ? TM * PW * 2 : 16, 8 * PW * 2, PW * 2);
-            tc_mma_bf16(tmem + C::ACC0 + ab * RP, ad, bd, id_acc, (first && part == 0 && kk == 0) ? 0u : 1u);
+            const uint64_t bd = tc_desc(bl + part * blob_tile(RP) + kk * 16 * PW * 2,
+                                        (C::HL || RP > PW) ? TM * PW * 2 : 16, 8 * PW * 2, PW * 2);
+            tc_mma_bf16(tmem + C::ACC0 + ab * C::AW, ad, bd, id_acc, (first && part == 0 && kk == 0) ? 0u : 1u);
           }
+        tc_commit(&bempty[sb]);
         tc_commit(kDX ? &xfree[s] : &empty[s]);
         if (last) {
           tc_commit(&afull[ab]);
@@ -634,7 +674,7 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
         // warp stores its 32 rows with TMA (rows past M and columns past K are
         // clipped by the store)
         const int db = g & 1, s = g % NS;
-        uint8_t *st = ring + s * C::STAGE;
+        uint8_t *st = ring + s * C::IN_B;
         tc_fence_after();
         const int64_t grow = (int64_t)t * TM + row;
         const __nv_bfloat16 *dxr = p.dX + grow * p.lddx;
@@ -692,7 +732,24 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
       for (int j = 0; j < RP; ++j) v[j] = 0.f;
       if (ok) {
         tc_fence_after();
-        tmem_row<RP>(tl + C::ACC0 + ab * RP, v);
+        tmem_row<RP>(tl + C::ACC0 + ab * C::AW, v);
+        if constexpr (C::HL) {
+          // the lo half, added in 16- or 32-column pieces
+          if constexpr (RP == 16) {
+            float w[16];
+            tmem_ld16(tl + C::ACC0 + ab * C::AW + RP, w);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] += w[j];
+          } else {
+#pragma unroll
+            for (int c = 0; c < RP; c += 32) {
+              float w[32];
+              tmem_ld32(tl + C::ACC0 + ab * C::AW + RP + c, w);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[c + j] += w[j];
+            }
+          }
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&aempty[ab]);
