@@ -123,6 +123,27 @@ __device__ __forceinline__ bool reduce_segment(int64_t U, int G, int i, int64_t 
   return last;
 }
 
+// Row `row` of 128-row block `blk` of a saved fp32 h (columns j < r; zero past r
+// and past M) into that block's hi / lo blob tiles.
+template <int RP>
+__device__ __forceinline__ void hrow_to_blob(const float *__restrict__ h, int64_t ldh, int64_t M, int r, int64_t blk,
+                                             int row, uint8_t *blob) {
+  uint8_t *bhi = blob + blk * (int64_t)(2 * blob_tile(RP)), *blo = bhi + blob_tile(RP);
+  const int64_t m = blk * TM + row;
+#pragma unroll
+  for (int col = 0; col < RP; col += 8) {
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = m < M && col + k < r ? h[m * ldh + col + k] : 0.f;
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) split_bf16(v[2 * k], v[2 * k + 1], hi[k], lo[k]);
+    const uint32_t o = blob_off<RP>(row, col);
+    *reinterpret_cast<uint4 *>(bhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4 *>(blo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
 // ============================================================================= rows
 template <int RP, bool kWMN>
 struct RowsCfg {
@@ -234,6 +255,12 @@ __global__ void __launch_bounds__(NTHR, 1) rows_kernel(const __grid_constant__ C
     int seg = 0;
     bool ok = true;   // after a timed-out wait: skip the work, keep the barrier sequence
     const int64_t rb0 = u0 < u1 ? u0 / nc : 0, rb1 = u0 < u1 ? (u1 - 1) / nc : -1;
+    if (p.hin != nullptr) {
+      // the saved h as a blob for a later pass: the epilogue is idle until its
+      // first block's accumulator is complete
+      const int64_t nrb = ((int64_t)p.M + TM - 1) / TM;
+      for (int64_t blk = i; blk < nrb; blk += gridDim.x) hrow_to_blob<RP>(p.hin, p.ldhin, p.M, p.r, blk, row, p.hblob);
+    }
     for (int64_t rb = rb0; rb <= rb1; ++rb, ++seg) {
       const int b = seg & 1;
       if (ok) ok = wait_warp(&afull[b], (seg >> 1) & 1);
@@ -782,31 +809,6 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
   }
 }
 
-// ============================================================================= saved h -> blob
-// The saved h (fp32 [M][ldh], columns j < r; zero past r and past M) as a blob,
-// one 128-row block per CTA.
-template <int RP>
-__global__ void __launch_bounds__(256) hblob_kernel(const float *__restrict__ h, int64_t ldh, int64_t M, int r,
-                                                    uint8_t *blob) {
-  pdl_wait();
-  uint8_t *bhi = blob + (size_t)blockIdx.x * 2 * blob_tile(RP), *blo = bhi + blob_tile(RP);
-  const int64_t m0 = (int64_t)blockIdx.x * TM;
-  for (int e = threadIdx.x; e < TM * RP / 8; e += blockDim.x) {
-    const int row = e / (RP / 8), col = 8 * (e % (RP / 8));
-    const int64_t m = m0 + row;
-    float v[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) v[k] = m < M && col + k < r ? h[m * ldh + col + k] : 0.f;
-    uint32_t hi[4], lo[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) split_bf16(v[2 * k], v[2 * k + 1], hi[k], lo[k]);
-    const uint32_t o = blob_off<RP>(row, col);
-    *reinterpret_cast<uint4 *>(bhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4 *>(blo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-  }
-  pdl_launch_dependents();
-}
-
 }  // namespace tc
 
 // ----------------------------------------------------------------------------- host side
@@ -872,10 +874,12 @@ size_t ws_col(int64_t M, int64_t C) {
 }
 
 // h = In * W (W = A: K-major, kWMN = false; W = B^T from B in PEFT layout: kWMN = true)
-// into the blob (and fp32 rows into hout when given).
+// into the blob (and fp32 rows into hout when given); with hin, the saved fp32 h
+// [M][ldhin] is also converted into the blob hblob.
 template <int RP, bool kWMN>
 lora_status_t launch_rows(const void *in, int64_t ld_in, int64_t M, int64_t Cdim, int r, const CUtensorMap &tW,
-                          int *counters, WsCarver &ws, uint8_t **blob_out, float *hout, int64_t ldh, cudaStream_t st) {
+                          int *counters, WsCarver &ws, uint8_t **blob_out, float *hout, int64_t ldh, cudaStream_t st,
+                          const float *hin = nullptr, int64_t ldhin = 0, uint8_t *hblob = nullptr) {
   using Cf = RowsCfg<RP, kWMN>;
   auto kern = rows_kernel<RP, kWMN>;
   LORA_CUDA(ensure_smem((const void *)kern, Cf::BYTES));
@@ -898,6 +902,9 @@ lora_status_t launch_rows(const void *in, int64_t ld_in, int64_t M, int64_t Cdim
   p.blob = blob;
   p.hout = hout;
   p.ldh = ldh;
+  p.hin = hin;
+  p.ldhin = ldhin;
+  p.hblob = hblob;
   LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(NTHR), Cf::BYTES, st, 1, true, tIn, tW, p));
   *blob_out = blob;
   return LORA_OK;
@@ -1015,9 +1022,10 @@ lora_status_t forward_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStr
   return launch_expand<RP>(blob, a, tB, st);
 }
 
-// dyb blob, then dX and dA; cnt holds ceil(M/128) + ceil(K/128) counters
+// dyb blob, then dX and dA; cnt holds ceil(M/128) + ceil(K/128) counters.  With
+// hblob, the dyb pass also writes the blob of the saved h (a.h) there.
 template <int RP>
-lora_status_t dxda_rp(const SingleArgs &a, int *cnt, WsCarver &carver, cudaStream_t st) {
+lora_status_t dxda_rp(const SingleArgs &a, int *cnt, WsCarver &carver, cudaStream_t st, uint8_t *hblob = nullptr) {
   SingleLayout lay = plan_layout(a, true, true);
   const void *Ac = nullptr, *Bc = nullptr;
   LORA_TRY(pack_tc(a, lay, carver, &Ac, &Bc, st));
@@ -1025,7 +1033,8 @@ lora_status_t dxda_rp(const SingleArgs &a, int *cnt, WsCarver &carver, cudaStrea
   if (!map_ac_tc(&tA, Ac, a.K, a.r, lay.lda, RP) || !map_bc_tc(&tB, Bc, a.L, a.r, lay.ldb, RP))
     return LORA_ERR_ALIGNMENT;
   uint8_t *blob = nullptr;
-  LORA_TRY((launch_rows<RP, true>(a.dY, a.lddy, a.M, a.L, a.r, tB, cnt, carver, &blob, nullptr, 0, st)));
+  LORA_TRY((launch_rows<RP, true>(a.dY, a.lddy, a.M, a.L, a.r, tB, cnt, carver, &blob, nullptr, 0, st,
+                                   hblob ? (const float *)a.h : nullptr, a.ldh, hblob)));
   return launch_col<RP, true>(a.X, a.ldx, a.M, a.K, a.r, blob, &tA, a.scale, a.dA, a.sdA_k, a.sdA_r, a.grad_lo != 0,
                               a.dX, a.lddx, a.dx_acc != 0, cnt + ceil_div(a.M, TM), carver, st);
 }
@@ -1067,11 +1076,9 @@ lora_status_t backward_op(const SingleArgs &a, WsCarver &carver, cudaStream_t st
   const int64_t nrb = ceil_div(a.M, TM), nkb = ceil_div(a.K, TM);
   int *cnt = take_counters(carver, nrb + nkb + ceil_div(a.L, TM), st, &e);
   LORA_TRY(e);
-  LORA_TRY(dxda_rp<RP>(a, cnt, carver, st));
   uint8_t *hb = (uint8_t *)carver.take((size_t)nrb * 2 * blob_tile(RP));
   if (!hb) return LORA_ERR_WORKSPACE;
-  LORA_CUDA(launch(hblob_kernel<RP>, dim3((unsigned)nrb), dim3(256), 0, st, 1, true, (const float *)a.h, a.ldh, a.M,
-                   a.r, hb));
+  LORA_TRY(dxda_rp<RP>(a, cnt, carver, st, hb));
   return db_from_blob<RP>(a, hb, cnt + nrb + nkb, carver, st);
 }
 
