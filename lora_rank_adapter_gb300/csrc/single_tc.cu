@@ -109,10 +109,24 @@ __device__ __forceinline__ bool reduce_segment(int64_t U, int G, int i, int64_t 
   named_bar_sync(1, 128);
   const bool last = *s_flag != 0;
   if (last) {
+    // the partials in CTA order; at RP <= 64 this CTA's own one is taken from
+    // v rather than reloaded (the stored copy holds the same values, so the
+    // result does not depend on which CTA finishes last)
     __threadfence();
+    float own[RP <= 64 ? RP : 1];
 #pragma unroll
-    for (int j = 0; j < RP; ++j) v[j] = 0.f;
+    for (int j = 0; j < RP; ++j) {
+      if constexpr (RP <= 64) own[j] = v[j];
+      v[j] = 0.f;
+    }
     for (int c = first; c <= last_cta; ++c) {
+      if constexpr (RP <= 64) {
+        if (c == i) {
+#pragma unroll
+          for (int j = 0; j < RP; ++j) v[j] += own[j];
+          continue;
+        }
+      }
       const float *pc = part + part_slot(U, G, c, g, n) * TM * RP + row;
 #pragma unroll
       for (int j = 0; j < RP; ++j) v[j] += __ldcg(pc + j * TM);
@@ -288,9 +302,16 @@ __global__ void __launch_bounds__(NTHR, 1) rows_kernel(const __grid_constant__ C
       const int64_t grow = rb * TM + row;
       if (p.hout != nullptr && grow < p.M) {
         float *hr = p.hout + grow * p.ldh;
+        if (p.h_vec4) {
+          // 16-byte stores: a quarter of the store instructions (each lane writes its own row)
 #pragma unroll
-        for (int j = 0; j < RP; ++j)
-          if (j < p.r) hr[j] = v[j];
+          for (int j = 0; j < RP; j += 4)
+            if (j < p.r) *reinterpret_cast<float4 *>(hr + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < RP; ++j)
+            if (j < p.r) hr[j] = v[j];
+        }
       }
     }
   }
@@ -902,6 +923,7 @@ lora_status_t launch_rows(const void *in, int64_t ld_in, int64_t M, int64_t Cdim
   p.blob = blob;
   p.hout = hout;
   p.ldh = ldh;
+  p.h_vec4 = hout != nullptr && (reinterpret_cast<uintptr_t>(hout) & 15) == 0 && ldh % 4 == 0 && r % 4 == 0;
   p.hin = hin;
   p.ldhin = ldhin;
   p.hblob = hblob;

@@ -22,6 +22,7 @@ struct TcRowsArgs {
   uint8_t *blob;             // out: hi / lo bf16 tiles per row block
   float *hout;               // out (optional): fp32 rows [M][ldh], columns < r
   int64_t ldh;
+  int h_vec4;                // hout rows written as float4 (16-byte aligned rows, r % 4 == 0)
   const float *hin;          // in (optional): a saved fp32 h [M][ldhin], converted
   int64_t ldhin;             //   to a blob at hblob by the epilogue warps before
   uint8_t *hblob;            //   their first block (one 128-row block per CTA in turn)
