@@ -72,11 +72,17 @@ __device__ __forceinline__ uint32_t blob_off(int row, int col) {
 }
 
 // Partial sums are stored column-major ([RP columns][128 rows]): a warp's
-// accesses of one column are 32 consecutive floats.
+// accesses of one column are 32 consecutive floats.  They are stored with an
+// L2 evict-last policy (a few MB in all): the CTA that finishes the block reads
+// them back, usually at the end of the pass, after the HBM stream has gone by.
 template <int RP>
 __device__ __forceinline__ void store_partial(float *part, int row, const float *v) {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
 #pragma unroll
-  for (int j = 0; j < RP; ++j) __stcg(part + j * TM + row, v[j]);
+  for (int j = 0; j < RP; ++j)
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(part + j * TM + row), "f"(v[j]), "l"(pol)
+                 : "memory");
 }
 // RP accumulator columns of this thread's TMEM lane.
 template <int RP>
