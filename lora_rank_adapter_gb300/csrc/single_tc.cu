@@ -811,7 +811,15 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
       ++seg;
       if (!reduce_segment<RP>(p.U, p.G, i, cb, nt, p.part, p.counters + cb, row, v, s_flag)) continue;
       const int64_t c = (int64_t)cb * TM + row;
-      if (c < p.C) {
+      if (c < p.C && p.out_vec4) {
+        // fp32 rows of the output contiguous and 16-byte aligned: 16-byte stores
+        float *orow = reinterpret_cast<float *>(p.out) + c * p.out_sc;
+#pragma unroll
+        for (int j = 0; j < RP; j += 4)
+          if (j < p.r)
+            *reinterpret_cast<float4 *>(orow + j) = make_float4(p.out_scale * v[j], p.out_scale * v[j + 1],
+                                                                p.out_scale * v[j + 2], p.out_scale * v[j + 3]);
+      } else if (c < p.C) {
 #pragma unroll
         for (int j = 0; j < RP; ++j) {
           if (j >= p.r) break;
@@ -969,6 +977,8 @@ lora_status_t launch_col(const void *in, int64_t ld_in, int64_t M, int64_t Cdim,
   p.out_sc = out_sc;
   p.out_sj = out_sj;
   p.out_bf16 = out_bf16 ? 1 : 0;
+  p.out_vec4 = !out_bf16 && out_sj == 1 && out_sc % 4 == 0 && r % 4 == 0 &&
+               (reinterpret_cast<uintptr_t>(out) & 15) == 0;
   p.dX = (__nv_bfloat16 *)dX;
   p.lddx = lddx;
   LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(NTHR), Cf::BYTES, st, 1, true, tIn, kDX ? *tAc : tIn, kDX ? tDX : tIn,

@@ -42,6 +42,7 @@ struct TcColArgs {
   void *out;                 // out(c, j) at out[c * out_sc + j * out_sj], fp32 or bf16
   int64_t out_sc, out_sj;
   int out_bf16;
+  int out_vec4;              // fp32 output rows contiguous (out_sj = 1) and 16-byte aligned
   __nv_bfloat16 *dX;         // dX [M][lddx] (kDX)
   int64_t lddx;
 };
