@@ -367,8 +367,9 @@ __global__ void __launch_bounds__(NTHR, 1)
 // 256 rows of b as boxes of 64, 32, 16 and 8 entries (one TMA row request per
 // box row; swizzled so that the fragment loads hit distinct banks).  Compute
 // warp w takes the 8-column groups w, w + 8, w + 16, w + 24 of each unit:
-// mma.sync with A = the tile's h rows (bf16 high part and residual, so that h
-// keeps about fp32 precision) and B = the b pieces (entries past the rank
+// mma.sync with A = the tile's h rows rounded to bf16 once (relative error
+// 2^-9 per term, well inside what the bf16 result of the add holds, as in the
+// prefill expand) and B = the b pieces (entries past the rank
 // masked: b may hold anything there), then y += scal * D in shared memory;
 // after a barrier one thread stores the updated rows with TMA stores.
 constexpr int ECB = 256;                     // output columns of a unit
@@ -614,9 +615,9 @@ __global__ void __launch_bounds__(NTHR_E, 1)
             bmsk[ks][hf] = j >= rank ? 0u : j + 1 >= rank ? 0xffffu : 0xffffffffu;
           }
       }
-      // A fragments a0 / a2 of the tile's h rows: high part and residual
+      // A fragments a0 / a2 of the tile's h rows in bf16
       const int kst = (r8 + 15) / 16, ng = r8 / 8;
-      uint32_t ahi[KS][2], alo[KS][2];
+      uint32_t ahi[KS][2];
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
@@ -624,10 +625,7 @@ __global__ void __launch_bounds__(NTHR_E, 1)
           const int j = 16 * ks + 8 * hf + gt;   // below 16 kst <= EHR when ks < kst
           float2 v = make_float2(0.f, 0.f);
           if (ks < kst && gm < kDecTokens) v = *reinterpret_cast<const float2 *>(&H->h[gm][j]);
-          const float v0 = v.x, v1 = v.y;
-          const __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
-          ahi[ks][hf] = pack_bf16(v0, v1);
-          alo[ks][hf] = pack_bf16(v0 - __bfloat162float(h0), v1 - __bfloat162float(h1));
+          ahi[ks][hf] = pack_bf16(v.x, v.y);
         }
       uint8_t *sy = ring + s * STAGE;
       const uint8_t *sb = sy + nq * EYA;
@@ -646,9 +644,8 @@ __global__ void __launch_bounds__(NTHR_E, 1)
               b[hf] = bmsk[ks][hf] ? *reinterpret_cast<const uint32_t *>(bu + boff[ks][hf] + nt * bstr[ks][hf]) &
                                          bmsk[ks][hf]
                                    : 0u;
-            const uint32_t ah[4] = {ahi[ks][0], 0u, ahi[ks][1], 0u}, al[4] = {alo[ks][0], 0u, alo[ks][1], 0u};
+            const uint32_t ah[4] = {ahi[ks][0], 0u, ahi[ks][1], 0u};
             mma_bf16(acc, ah, b[0], b[1]);
-            mma_bf16(acc, al, b[0], b[1]);
           }
           if (gm < len) {
             uint32_t *yp = reinterpret_cast<uint32_t *>(sy + (kq * kDecTokens + gm) * EYB + (8 * nt + gt) * 2);
