@@ -620,7 +620,12 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();
+  // The dB pass of lora_backward needs nothing from the dX pass before it (its
+  // dY and h blob were complete before that pass got past its own wait): it
+  // starts while the dX pass's last CTAs finish and waits for that pass only
+  // before exiting, so that it still completes after it.
+  if (p.wait_first) pdl_wait();
+  if (kDX) pdl_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -835,7 +840,8 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
       bulk_wait_all();
     }
   }
-  pdl_launch_dependents();
+  if (!p.wait_first) pdl_wait();
+  if (!kDX) pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -950,7 +956,8 @@ lora_status_t launch_rows(const void *in, int64_t ld_in, int64_t M, int64_t Cdim
 template <int RP, bool kDX>
 lora_status_t launch_col(const void *in, int64_t ld_in, int64_t M, int64_t Cdim, int r, const uint8_t *blob,
                          const CUtensorMap *tAc, float scale, void *out, int64_t out_sc, int64_t out_sj, bool out_bf16,
-                         void *dX, int64_t lddx, bool dx_acc, int *counters, WsCarver &ws, cudaStream_t st) {
+                         void *dX, int64_t lddx, bool dx_acc, int *counters, WsCarver &ws, cudaStream_t st,
+                         bool wait_first = true) {
   using Cf = ColCfg<RP, kDX>;
   auto kern = kDX ? (dx_acc ? col_kernel<RP, true, true> : col_kernel<RP, true, false>) : col_kernel<RP, false, false>;
   LORA_CUDA(ensure_smem((const void *)kern, Cf::BYTES));
@@ -981,6 +988,7 @@ lora_status_t launch_col(const void *in, int64_t ld_in, int64_t M, int64_t Cdim,
                (reinterpret_cast<uintptr_t>(out) & 15) == 0;
   p.dX = (__nv_bfloat16 *)dX;
   p.lddx = lddx;
+  p.wait_first = wait_first ? 1 : 0;
   LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(NTHR), Cf::BYTES, st, 1, true, tIn, kDX ? *tAc : tIn, kDX ? tDX : tIn,
                    p));
   return LORA_OK;
@@ -1077,11 +1085,13 @@ lora_status_t dxda_rp(const SingleArgs &a, int *cnt, WsCarver &carver, cudaStrea
                               a.dX, a.lddx, a.dx_acc != 0, cnt + ceil_div(a.M, TM), carver, st);
 }
 
-// dB from a blob of h; cnt holds ceil(L/128) counters
+// dB from a blob of h; cnt holds ceil(L/128) counters.  wait_first = false when
+// the previous launch neither writes the blob nor dY (the dX pass of lora_backward).
 template <int RP>
-lora_status_t db_from_blob(const SingleArgs &a, const uint8_t *hblob, int *cnt, WsCarver &carver, cudaStream_t st) {
+lora_status_t db_from_blob(const SingleArgs &a, const uint8_t *hblob, int *cnt, WsCarver &carver, cudaStream_t st,
+                           bool wait_first = true) {
   return launch_col<RP, false>(a.dY, a.lddy, a.M, a.L, a.r, hblob, nullptr, a.scale, a.dB, a.sdB_l, a.sdB_r,
-                               a.grad_lo != 0, nullptr, 0, false, cnt, carver, st);
+                               a.grad_lo != 0, nullptr, 0, false, cnt, carver, st, wait_first);
 }
 
 template <int RP>
@@ -1117,7 +1127,7 @@ lora_status_t backward_op(const SingleArgs &a, WsCarver &carver, cudaStream_t st
   uint8_t *hb = (uint8_t *)carver.take((size_t)nrb * 2 * blob_tile(RP));
   if (!hb) return LORA_ERR_WORKSPACE;
   LORA_TRY(dxda_rp<RP>(a, cnt, carver, st, hb));
-  return db_from_blob<RP>(a, hb, cnt + nrb + nkb, carver, st);
+  return db_from_blob<RP>(a, hb, cnt + nrb + nkb, carver, st, false);
 }
 
 template <typename F>

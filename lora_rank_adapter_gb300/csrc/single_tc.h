@@ -43,6 +43,7 @@ struct TcColArgs {
   int64_t out_sc, out_sj;
   int out_bf16;
   int out_vec4;              // fp32 output rows contiguous (out_sj = 1) and 16-byte aligned
+  int wait_first;            // wait for the previous launch at the start (else only before exiting)
   __nv_bfloat16 *dX;         // dX [M][lddx] (kDX)
   int64_t lddx;
 };
