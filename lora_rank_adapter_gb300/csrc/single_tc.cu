@@ -21,7 +21,7 @@
 //                  a "blob": the bf16 hi and lo parts (v ~= hi + lo to ~2^-17) of
 //                  the 128 x RP block, already in the swizzled layout the tensor
 //                  cores read, and optionally as fp32 rows (the saved h).
-//   expand_kernel  Y[m, l] += s * sum_j h[m, j] B[j, l] over (row block, 64-column
+//   expand_kernel  Y[m, l] += s * sum_j h[m, j] B[j, l] over (row block, 128-column
 //                  chunk of Y) units: h hi/lo from the blob, B^T chunks and Y tiles
 //                  by TMA, the product in TMEM, Y read-modify-written once.
 //   col_kernel     acc[c, :] = sum over rows m of In[m, c] * blob[m, :] for
@@ -346,25 +346,29 @@ __global__ void __launch_bounds__(NTHR, 1) rows_kernel(const __grid_constant__ C
 // ============================================================================= expand
 // Y[m, l] += s * (h_hi + h_lo)[m, :] . B^T[l, :]; four TMEM accumulators of 64
 // columns let the epilogue of one chunk overlap the MMAs of the next.
+// An expand unit covers EUC columns of Y: two 64-column Y boxes, a 128-row B^T
+// chunk, one N = 128 MMA per K step (fewer, larger units, as in the rows pass).
+constexpr int EUC = 2 * BOXC;
+
 template <int RP>
 struct ExpCfg {
   static constexpr int PW = pw_of(RP);
-  static constexpr int Y_B = TM * BOXC * 2;      // 16 KB
-  static constexpr int B_B = BOXC * RP * 2;      // B^T chunk [64 l][RP]
+  static constexpr int Y_B = TM * EUC * 2;       // 32 KB: two [128][64] boxes
+  static constexpr int B_B = EUC * RP * 2;       // B^T chunk: RP / PW panels of [128 l][PW]
   static constexpr int HB = 2 * blob_tile(RP);   // hi + lo of one row block
-  // blob buffers: a row block covers L / 64 chunks, so at r = 64 one buffer
+  // blob buffers: a row block covers L / 128 units, so at r = 64 one buffer
   // (a short stall when the row block changes) buys the ring more Y stages
   static constexpr int NB = RP >= 64 ? 1 : 2;
   // Y tiles and B^T chunks have rings of their own: a Y stage is held until its
   // tile has been stored, a B^T stage only until the MMAs have read it, and the
   // MMAs never wait for a Y tile.  The loader issues both in unit order, so it
-  // runs at most NBB + ND units ahead of the epilogue: NBB = NS - ND lets the Y
-  // ring fill.
-  static constexpr int ND = 4;
-  static constexpr int NS0 = (kRingBytes + 28 * 1024 - NB * HB + ND * B_B) / (Y_B + B_B);
+  // runs at most NBB + ND units ahead of the epilogue (not fewer than NS here).
+  static constexpr int ND = 4;                   // accumulators of 128 TMEM columns
+  static constexpr int NBB = 2;
+  static constexpr int NS0 = (kRingBytes + 28 * 1024 - NB * HB - NBB * B_B) / Y_B;
   static constexpr int NS = NS0 > 12 ? 12 : NS0;
-  static constexpr int NBB = NS - ND > 2 ? NS - ND : 2;
-  static constexpr int TMEM = 256;
+  static_assert(NS <= NBB + ND, "the loader must be able to fill the Y ring");
+  static constexpr int TMEM = 512;
   static constexpr int BYTES = 1024 + NB * HB + NS * Y_B + NBB * B_B + 1024;
   static_assert(BYTES <= 227 * 1024, "expand shared memory");
 };
@@ -432,13 +436,18 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
         const int g = (int)(u - u0), s = g % NS, sb = g % NBB;
         if (g >= NS && !mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) break;
         mbar_arrive_expect_tx(&full[s], C::Y_B);
-        tma_load_2d(ring + s * C::Y_B, &tmY, &full[s], lc * BOXC, (int)(rb * TM));
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_2d(ring + s * C::Y_B + hf * (TM * BOXC * 2), &tmY, &full[s], lc * EUC + hf * BOXC, (int)(rb * TM));
         if (g >= NBB && !mbar_wait(&bempty[sb], ((g / NBB) & 1) ^ 1)) break;
         uint8_t *bt = bring + sb * C::B_B;
         mbar_arrive_expect_tx(&bfull[sb], C::B_B);
 #pragma unroll
         for (int pp = 0; pp < RP / PW; ++pp)
-          tma_load_2d(bt + pp * (BOXC * PW * 2), &tmB, &bfull[sb], pp * PW, lc * BOXC);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_2d(bt + pp * (EUC * PW * 2) + hf * (BOXC * PW * 2), &tmB, &bfull[sb], pp * PW,
+                        lc * EUC + hf * BOXC);
         // the row block's blob after the unit's stage (which does not need it), so
         // that a buffer still read by the previous block's MMAs delays no Y copy
         if (rb != prev) {
@@ -453,7 +462,7 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = tc_idesc(TM, BOXC, false, false);
+      const uint32_t idesc = tc_idesc(TM, EUC, false, false);
       int64_t prev = -1;
       int hidx = 0, hb = 0;
       bool ok = true;
@@ -476,8 +485,8 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
           for (int qk = 0; qk < RP / 16; ++qk) {
             const int pan = (qk * 16) / PW, in = ((qk * 16) % PW) * 2;
             const uint64_t ad = tc_desc(hh + part * blob_tile(RP) + pan * (TM * PW * 2) + in, 16, 8 * PW * 2, PW * 2);
-            const uint64_t bd = tc_desc(bb + pan * (BOXC * PW * 2) + in, 16, 8 * PW * 2, PW * 2);
-            tc_mma_bf16(tmem + b * BOXC, ad, bd, idesc, (part == 0 && qk == 0) ? 0u : 1u);
+            const uint64_t bd = tc_desc(bb + pan * (EUC * PW * 2) + in, 16, 8 * PW * 2, PW * 2);
+            tc_mma_bf16(tmem + b * EUC, ad, bd, idesc, (part == 0 && qk == 0) ? 0u : 1u);
           }
         tc_commit(&dfull[b]);
         tc_commit(&bempty[sb]);
@@ -502,30 +511,37 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
       const int g = (int)(u - u0), s = g % NS, b = g % ND;
       if (!wait_warp(&dfull[b], (g / ND) & 1) || !wait_warp(&full[s], (g / NS) & 1)) break;
       tc_fence_after();
-      float acc[64];
-      tmem_ld32(tl + b * BOXC, acc);
-      tmem_ld32(tl + b * BOXC + 32, acc + 32);
-      tc_fence_before();
-      uint8_t *yt = ring + s * C::Y_B;
+      uint8_t *ys = ring + s * C::Y_B;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 *yp = reinterpret_cast<uint4 *>(yt + swz(row, c * 16, 128));
-        const uint4 yv = *yp;
-        const uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
-        uint32_t o[4];
+      for (int hf = 0; hf < 2; ++hf) {
+        float acc[64];
+        tmem_ld32(tl + b * EUC + hf * BOXC, acc);
+        tmem_ld32(tl + b * EUC + hf * BOXC + 32, acc + 32);
+        uint8_t *yt = ys + hf * (TM * BOXC * 2);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 y = unpack_bf16(w[e]);
-          o[e] = pack_bf16(y.x + scale * acc[8 * c + 2 * e], y.y + scale * acc[8 * c + 2 * e + 1]);
+        for (int c = 0; c < 8; ++c) {
+          uint4 *yp = reinterpret_cast<uint4 *>(yt + swz(row, c * 16, 128));
+          const uint4 yv = *yp;
+          const uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 y = unpack_bf16(w[e]);
+            o[e] = pack_bf16(y.x + scale * acc[8 * c + 2 * e], y.y + scale * acc[8 * c + 2 * e + 1]);
+          }
+          *yp = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        *yp = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      fence_proxy_async_smem();   // the TMA store reads what this warp wrote
+      tc_fence_before();
+      fence_proxy_async_smem();   // the TMA stores read what this warp wrote
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&dempty[b]);
         const int64_t rb = u / nl;
-        tma_store_2d(&tmYs, yt + q * 32 * 128, (int)(u % nl) * BOXC, (int)(rb * TM) + 32 * q);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+          tma_store_2d(&tmYs, ys + hf * (TM * BOXC * 2) + q * 32 * 128, (int)(u % nl) * EUC + hf * BOXC,
+                       (int)(rb * TM) + 32 * q);
         bulk_commit();
         if (pend >= 0) {
           bulk_wait_read1();
@@ -1012,7 +1028,7 @@ lora_status_t launch_expand(const uint8_t *blob, const SingleArgs &a, const CUte
   using Cf = ExpCfg<RP>;
   auto kern = expand_kernel<RP>;
   LORA_CUDA(ensure_smem((const void *)kern, Cf::BYTES));
-  const int64_t nrb = ceil_div(a.M, TM), nl = ceil_div(a.L, BOXC);
+  const int64_t nrb = ceil_div(a.M, TM), nl = ceil_div(a.L, EUC);
   const int G = grid_for(nrb * nl, (const void *)kern, Cf::BYTES, 1);
   CUtensorMap tY, tYs;
   if (!map_big128(&tY, a.Y, a.M, a.L, a.ldy) || !map_rows_box(&tYs, a.Y, a.M, a.L, a.ldy, 32))
