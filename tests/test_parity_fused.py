@@ -229,3 +229,42 @@ def test_backward_ex_degenerate_shapes():
                           dA2, dB2, flags=3)
     torch.cuda.synchronize()
     assert torch.equal(dX, dX0) and torch.all(dA == 0) and torch.all(dA2 == 0) and torch.all(dB2 == 0)
+
+
+def test_backward_then_dependent_launch_sees_dx():
+    """The dB pass of lora_backward starts before the dX pass has finished and
+    waits for it only before exiting: a launch right after the backward that
+    reads dX (here, a forward with dX as its input) must see all of it.  The
+    chain on one stream is compared with the same chain separated by full
+    synchronizations (c3-like widths, so the dX pass is long and the dB pass
+    short)."""
+    M, K, L, r = 4096, 4096, 1024, 64
+    spec = synth.single_spec("single_c3_down", M=M, K=K, L=L, r=r)
+    w = synth.make_single(spec, seed=21, device=DEV)
+    X, A, B, dY = w["X"], w["A"], w["B"], w["dY"]
+    s = spec["s"]
+    h = torch.empty((M, r), dtype=torch.float32, device=DEV)
+    Y = w["Y0"].clone()
+    lora.lora_forward_h(X, A, B, Y, s, h)
+    torch.cuda.synchronize()
+    A2 = (A.float() * 0.5).to(A.dtype)
+    B2 = torch.randn((r, 512), device=DEV).to(B.dtype)
+
+    def chain(sync):
+        dX = torch.full_like(X, float("nan"))
+        dA = torch.empty((K, r), dtype=torch.float32, device=DEV)
+        dB = torch.empty((r, L), dtype=torch.float32, device=DEV)
+        Y2 = torch.zeros((M, 512), dtype=X.dtype, device=DEV)
+        lora.lora_backward(X, dY, A, B, h, s, dX, dA, dB)
+        if sync:
+            torch.cuda.synchronize()
+        lora.lora_forward(dX, A2, B2, Y2, 1.0)
+        torch.cuda.synchronize()
+        return dX, Y2
+
+    dx_sync, y_sync = chain(True)
+    for _ in range(5):
+        dx_chain, y_chain = chain(False)
+        assert torch.equal(dx_chain, dx_sync)
+        assert torch.equal(y_chain, y_sync)
+    assert torch.isfinite(y_sync.float()).all()
