@@ -101,45 +101,65 @@ __device__ __forceinline__ void tmem_row(uint32_t taddr, float *v) {
 // The epilogue's end of the segment of group g (units [g n, (g + 1) n)) that CTA
 // i computed: either the group is all this CTA's (no partial), or the partial
 // goes to the workspace and the last CTA of the group to finish adds the
-// partials of all its CTAs in CTA order.  Returns true when this CTA then holds
-// the group's full sum in v.  Called by the four epilogue warps together.
+// partials of all its CTAs in CTA order, starting from 0.  Returns true when
+// this CTA then holds the group's full sum in v.  Called by the four epilogue
+// warps together (`leader` is the first thread of the four).
+//
+// The group's first CTA reaches the group with the last units of its range, the
+// others with their first units, so the first CTA usually finishes it last.  It
+// therefore takes its ticket before storing anything: it adds kFirstTicket; if
+// every other CTA has already stored (the count it sees is theirs), it is the
+// last one, and its own partial, the first term of the sum, never leaves v.
+// Otherwise it stores like the others, which add 1 after storing, and the CTA
+// whose addition completes kFirstTicket + (number of CTAs) is the last one: by
+// then every partial is stored, and it reloads them all, its own included (the
+// stored copy holds the same values, so the result does not depend on which
+// CTA finishes last).  No CTA waits for another either way.
+constexpr int kFirstTicket = 1 << 16;
 template <int RP>
 __device__ __forceinline__ bool reduce_segment(int64_t U, int G, int i, int64_t g, int64_t n, float *part,
-                                               int *counter, int row, float *v, int *s_flag) {
+                                               int *counter, int row, float *v, int *s_flag,
+                                               int leader = EPI0 * 32) {
   const int first = sk_cta(U, G, g * n), last_cta = sk_cta(U, G, (g + 1) * n - 1);
   if (first == last_cta) return true;
+  const int others = last_cta - first;
+  bool last;
+  if (i == first) {
+    if (threadIdx.x == leader) *s_flag = atomicAdd(counter, kFirstTicket) == others;
+    named_bar_sync(1, 128);
+    last = *s_flag != 0;
+    named_bar_sync(1, 128);
+    if (last) {
+      __threadfence();
+#pragma unroll
+      for (int j = 0; j < RP; ++j) v[j] = 0.f + v[j];   // as summed from 0 (the sign of a zero included)
+      for (int c = first + 1; c <= last_cta; ++c) {
+        const float *pc = part + part_slot(U, G, c, g, n) * TM * RP + row;
+#pragma unroll
+        for (int j = 0; j < RP; ++j) v[j] += __ldcg(pc + j * TM);
+      }
+      if (threadIdx.x == leader) *counter = 0;
+      return true;
+    }
+  }
   store_partial<RP>(part + part_slot(U, G, i, g, n) * TM * RP, row, v);
   __threadfence();
   named_bar_sync(1, 128);
-  if (threadIdx.x == EPI0 * 32) *s_flag = atomicAdd(counter, 1) == last_cta - first;
+  if (threadIdx.x == leader) *s_flag = atomicAdd(counter, 1) == kFirstTicket + others;
   named_bar_sync(1, 128);
-  const bool last = *s_flag != 0;
+  last = *s_flag != 0;
   if (last) {
-    // the partials in CTA order; at RP <= 64 this CTA's own one is taken from
-    // v rather than reloaded (the stored copy holds the same values, so the
-    // result does not depend on which CTA finishes last)
     __threadfence();
-    float own[RP <= 64 ? RP : 1];
 #pragma unroll
-    for (int j = 0; j < RP; ++j) {
-      if constexpr (RP <= 64) own[j] = v[j];
-      v[j] = 0.f;
-    }
+    for (int j = 0; j < RP; ++j) v[j] = 0.f;
     for (int c = first; c <= last_cta; ++c) {
-      if constexpr (RP <= 64) {
-        if (c == i) {
-#pragma unroll
-          for (int j = 0; j < RP; ++j) v[j] += own[j];
-          continue;
-        }
-      }
       const float *pc = part + part_slot(U, G, c, g, n) * TM * RP + row;
 #pragma unroll
       for (int j = 0; j < RP; ++j) v[j] += __ldcg(pc + j * TM);
     }
-    if (threadIdx.x == EPI0 * 32) *counter = 0;   // ready for the next call
+    if (threadIdx.x == leader) *counter = 0;
   }
-  named_bar_sync(1, 128);   // s_flag is reused by the next segment
+  named_bar_sync(1, 128);
   return last;
 }
 
@@ -571,7 +591,14 @@ struct ColCfg {
   static constexpr int PW = pw_of(RP);
   static constexpr int IN_B = 2 * TM * BOXC * 2;   // two 64-column boxes: 32 KB
   static constexpr int BL_B = 2 * blob_tile(RP);   // hi + lo
-  static constexpr int AC_B = kDX ? 2 * RP * 128 : 0;   // A^T for dX: two [RP][64] boxes
+  // A^T of one column block for dX: two [RP][64] boxes.  At RP <= 64 two such
+  // buffers, so that the next column block's A^T loads while the MMAs still read
+  // the current one and the In stream goes on (the ring keeps its stages); at
+  // RP = 128 one (a second would cost an In stage): there the loader waits at a
+  // column block's start for the MMAs of the one before.
+  static constexpr int AC1 = 2 * RP * 128;
+  static constexpr int NAC = kDX ? (RP <= 64 ? 2 : 1) : 0;
+  static constexpr int AC_B = NAC * AC1;
   static constexpr int SPACE = kRingBytes + 28 * 1024 - AC_B;
   // In tiles and blobs have rings of their own.  With dX an In stage is held
   // until the dX tile written over it has been stored, a blob stage only until
@@ -589,11 +616,19 @@ struct ColCfg {
   static constexpr int ACC0 = kDX ? 2 * TM : 0;   // first TMEM column of the accumulators
   static constexpr int BYTES = 1024 + NX * IN_B + NBL * BL_B + AC_B + 1024;
   static_assert(BYTES <= 227 * 1024, "column pass shared memory");
+  // With dX at RP <= 64 the accumulators have four epilogue warps of their own
+  // (warps 6-9, the same TMEM lane quarters as warps 2-5): the read-out, the
+  // partial-sum stores and the fences of a column block's end then never hold
+  // the dX tiles, which warps 2-5 drain.  (A fence waits behind the SM's loads
+  // in flight: microseconds in the middle of the stream.)  At RP = 128 the
+  // accumulator row takes the registers that ten warps would not leave.
+  static constexpr bool SPLIT = kDX && RP <= 64;
+  static constexpr int NT = SPLIT ? 320 : NTHR;
   static_assert(2 * AW + (kDX ? 2 * TM : 0) <= 512, "column pass tensor memory");
 };
 
 template <int RP, bool kDX, bool kAccX>
-__global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CUtensorMap tmIn,
+__global__ void __launch_bounds__(ColCfg<RP, kDX>::NT, 1) col_kernel(const __grid_constant__ CUtensorMap tmIn,
                                                       const __grid_constant__ CUtensorMap tmAc,
                                                       const __grid_constant__ CUtensorMap tmDX, TcColArgs p) {
   using C = ColCfg<RP, kDX>;
@@ -610,9 +645,9 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
   uint64_t *aempty = afull + 2;
   uint64_t *dfull = aempty + 2;    // [2] dX tiles
   uint64_t *dempty = dfull + 2;
-  uint64_t *acfull = dempty + 2;   // A^T tile loaded
-  uint64_t *acempty = acfull + 1;  // A^T tile no longer read
-  uint64_t *mdone = acempty + 1;
+  uint64_t *acfull = dempty + 2;   // [2] A^T buffer loaded
+  uint64_t *acempty = acfull + 2;  // [2] A^T buffer no longer read
+  uint64_t *mdone = acempty + 2;
   uint64_t *xfree = mdone + 1;     // [NS] the MMAs no longer read the stage's In tile
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfree + NS);
   int *s_flag = reinterpret_cast<int *>(tmem_slot + 1);
@@ -639,8 +674,10 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
       mbar_init(&dfull[b], 1);
       mbar_init(&dempty[b], 4);
     }
-    mbar_init(acfull, 1);
-    mbar_init(acempty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acfull[b], 1);
+      mbar_init(&acempty[b], 1);
+    }
     mbar_init(mdone, 1);
     fence_barrier_init();
   }
@@ -667,10 +704,13 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
       for (int64_t u = u0; u < u1; ++u) {
         const int cb = (int)(u / nt), t = (int)(u % nt);
         if (kDX && (u == u0 || t == 0)) {
-          if (seg >= 1 && !mbar_wait(acempty, (seg - 1) & 1)) break;
-          mbar_arrive_expect_tx(acfull, C::AC_B);
-          tma_load_2d(acbuf, &tmAc, acfull, cb * 2 * BOXC, 0);
-          tma_load_2d(acbuf + RP * 128, &tmAc, acfull, cb * 2 * BOXC + BOXC, 0);
+          // column block `seg` of the range uses A^T buffer seg % NAC
+          const int ab = C::NAC == 2 ? (seg & 1) : 0, use = C::NAC == 2 ? seg >> 1 : seg;
+          if (use >= 1 && !mbar_wait(&acempty[ab], (use - 1) & 1)) break;
+          uint8_t *ac = acbuf + ab * C::AC1;
+          mbar_arrive_expect_tx(&acfull[ab], C::AC1);
+          tma_load_2d(ac, &tmAc, &acfull[ab], cb * 2 * BOXC, 0);
+          tma_load_2d(ac + RP * 128, &tmAc, &acfull[ab], cb * 2 * BOXC + BOXC, 0);
           ++seg;
         }
         const int g = (int)(u - u0), s = g % NS, sb = g % NBL;
@@ -697,7 +737,8 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
         const int ab = seg & 1;
         if (first) {
           if (seg >= 2 && !(ok = mbar_wait(&aempty[ab], ((seg >> 1) & 1) ^ 1))) break;
-          if (kDX && !(ok = mbar_wait(acfull, seg & 1))) break;
+          if (kDX && !(ok = mbar_wait(&acfull[C::NAC == 2 ? (seg & 1) : 0], (C::NAC == 2 ? seg >> 1 : seg) & 1)))
+            break;
         }
         if (!(ok = mbar_wait(&full[s], (g / NS) & 1))) break;
         if (!(ok = mbar_wait(&bfull[sb], (g / NBL) & 1))) break;
@@ -707,7 +748,7 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
         const uint32_t st = smem_u32(ring + s * C::IN_B), bl = smem_u32(bring + sb * C::BL_B);
         if (kDX) {
           // dX tile [128 rows][128 columns] = (dyb_hi + dyb_lo) * A^T
-          const uint32_t ac = smem_u32(acbuf);
+          const uint32_t ac = smem_u32(acbuf + (C::NAC == 2 ? (seg & 1) : 0) * C::AC1);
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
@@ -735,7 +776,7 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
         tc_commit(kDX ? &xfree[s] : &empty[s]);
         if (last) {
           tc_commit(&afull[ab]);
-          if (kDX) tc_commit(acempty);
+          if (kDX) tc_commit(&acempty[C::NAC == 2 ? (seg & 1) : 0]);
           ++seg;
         }
       }
@@ -746,17 +787,18 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
   } else {
     const int q = warp & 3, row = 32 * q + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+    // with SPLIT warps 2-5 drain the dX tiles and warps 6-9 the accumulators
+    const bool dxw = kDX && (!C::SPLIT || warp < 6);
+    const int leader = C::SPLIT ? 6 * 32 : EPI0 * 32;
     int seg = 0;
     bool ok = true;   // after a timed-out wait: skip the work, keep the barrier sequence
     int pend = -1;    // stage whose dX store may still be reading it
     float v[RP];
-    for (int64_t u = u0; u < u1; ++u) {
-      const int g = (int)(u - u0);
-      const int cb = (int)(u / nt), t = (int)(u % nt);
-      const bool last = u == u1 - 1 || t == nt - 1;
-      if (kDX && ok) ok = wait_warp(&dfull[g & 1], (g >> 1) & 1);
-      if (kDX && ok) ok = wait_warp(&xfree[g % NS], (g / NS) & 1);
-      if (kDX && ok) {
+    // unit u's dX tile (kDX)
+    auto dx_unit = [&](int g, int cb, int t) {
+      if (ok) ok = wait_warp(&dfull[g & 1], (g >> 1) & 1);
+      if (ok) ok = wait_warp(&xfree[g % NS], (g / NS) & 1);
+      if (ok) {
         // the dX tile: scaled (and added to the old dX), rounded to bf16 and
         // written over the stage's In tile (same swizzled layout), then each
         // warp stores its 32 rows with TMA (rows past M and columns past K are
@@ -813,7 +855,9 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
           pend = s;
         }
       }
-      if (!last) continue;
+    };
+    // the end of column block cb: its accumulator, the block reduction, the output rows
+    auto acc_end = [&](int cb) {
       const int ab = seg & 1;
       if (ok) ok = wait_warp(&afull[ab], (seg >> 1) & 1);
 #pragma unroll
@@ -843,7 +887,7 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
         if (lane == 0) mbar_arrive(&aempty[ab]);
       }
       ++seg;
-      if (!reduce_segment<RP>(p.U, p.G, i, cb, nt, p.part, p.counters + cb, row, v, s_flag)) continue;
+      if (!reduce_segment<RP>(p.U, p.G, i, cb, nt, p.part, p.counters + cb, row, v, s_flag, leader)) return;
       const int64_t c = (int64_t)cb * TM + row;
       if (c < p.C && p.out_vec4) {
         // fp32 rows of the output contiguous and 16-byte aligned: 16-byte stores
@@ -862,8 +906,23 @@ __global__ void __launch_bounds__(NTHR, 1) col_kernel(const __grid_constant__ CU
           else reinterpret_cast<float *>(p.out)[o] = p.out_scale * v[j];
         }
       }
+    };
+    if (C::SPLIT) {
+      for (int64_t u = u0; u < u1; ++u) {
+        const int g = (int)(u - u0);
+        const int cb = (int)(u / nt), t = (int)(u % nt);
+        if (dxw) dx_unit(g, cb, t);
+        else if (u == u1 - 1 || t == nt - 1) acc_end(cb);
+      }
+    } else {
+      for (int64_t u = u0; u < u1; ++u) {
+        const int g = (int)(u - u0);
+        const int cb = (int)(u / nt), t = (int)(u % nt);
+        if (kDX) dx_unit(g, cb, t);
+        if (u == u1 - 1 || t == nt - 1) acc_end(cb);
+      }
     }
-    if (kDX && lane == 0) {
+    if (dxw && lane == 0) {
       bulk_wait_read_all();
       if (pend >= 0) mbar_arrive(&empty[pend]);
       bulk_wait_all();
@@ -922,8 +981,8 @@ bool map_bc_tc(CUtensorMap *m, const void *p, int64_t L, int r, int64_t ldb, int
 // sizes depend on the arguments only.
 constexpr int kMinUnits = 8;
 constexpr int kMaxGrid = 160;
-int grid_for(int64_t units, const void *kern, size_t smem, int min_units) {
-  const int occ = occupancy(kern, NTHR, smem);
+int grid_for(int64_t units, const void *kern, size_t smem, int min_units, int threads = NTHR) {
+  const int occ = occupancy(kern, threads, smem);
   return (int)std::max<int64_t>(
       1, std::min<int64_t>({ceil_div(units, min_units), (int64_t)occ * num_sms(), (int64_t)kMaxGrid}));
 }
@@ -991,7 +1050,7 @@ lora_status_t launch_col(const void *in, int64_t ld_in, int64_t M, int64_t Cdim,
   auto kern = kDX ? (dx_acc ? col_kernel<RP, true, true> : col_kernel<RP, true, false>) : col_kernel<RP, false, false>;
   LORA_CUDA(ensure_smem((const void *)kern, Cf::BYTES));
   const int64_t nt = ceil_div(M, TM), ncb = ceil_div(Cdim, TM);
-  const int G = grid_for(ncb * nt, (const void *)kern, Cf::BYTES, kMinUnits);
+  const int G = grid_for(ncb * nt, (const void *)kern, Cf::BYTES, kMinUnits, Cf::NT);
   float *part = (float *)ws.take((size_t)2 * G * TM * RP * 4);
   if (!part) return LORA_ERR_WORKSPACE;
   CUtensorMap tIn, tDX;
@@ -1018,7 +1077,7 @@ lora_status_t launch_col(const void *in, int64_t ld_in, int64_t M, int64_t Cdim,
   p.dX = (__nv_bfloat16 *)dX;
   p.lddx = lddx;
   p.wait_first = wait_first ? 1 : 0;
-  LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(NTHR), Cf::BYTES, st, 1, true, tIn, kDX ? *tAc : tIn, kDX ? tDX : tIn,
+  LORA_CUDA(launch(kern, dim3((unsigned)G), dim3(Cf::NT), Cf::BYTES, st, 1, true, tIn, kDX ? *tAc : tIn, kDX ? tDX : tIn,
                    p));
   return LORA_OK;
 }
