@@ -609,40 +609,69 @@ def run_gb300(args, rank, world, local_rank):
             "traffic": traffic_from_profiles(dom), "bytes_per_launch": step_parts[dom]["bytes"]}
     step_bytes = sum(p["bytes"] for p in step_parts.values())
 
-    # end to end: pinned host inputs in, results out, every step
+    # end to end: pinned host inputs in, results out, every step.  The copies in
+    # and out run on streams of their own, so that one step's results go out
+    # while the next step's inputs come in (host<->device copies in opposite
+    # directions overlap; one direction does not gain from splitting); alternate
+    # steps use two device copies of the step's input sets, and a copy's inputs
+    # go in only after that copy's previous results have been read out.
     E = min(args.e2e_steps, K)
-    host_in = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in h2d_d2h_tensors(S)[0]]
-               for S in sets]
-    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in h2d_d2h_tensors(S)[1]]
-                for S in sets]
-    used = sorted({(0 + j) % NSETS for j in range(len(ops))})
-
-    def e2e_step(i):
-        ks = sorted({(i + j) % NSETS for j in range(len(ops))})
-        for k in ks:
-            for dst, src in zip(h2d_d2h_tensors(sets[k])[0], host_in[k]):
-                dst.copy_(src, non_blocking=True)
-        step(i)
-        for k in ks:
-            for dst, src in zip(host_out[k], h2d_d2h_tensors(sets[k])[1]):
-                dst.copy_(src, non_blocking=True)
-
-    h2d = sum(t.numel() * t.element_size() for k in used for t in host_in[k])
-    d2h = sum(t.numel() * t.element_size() for k in used for t in host_out[k])
     e_ms = None
+    h2d = sum(t.numel() * t.element_size() for S in sets for t in h2d_d2h_tensors(S)[0])
+    d2h = sum(t.numel() * t.element_size() for S in sets for t in h2d_d2h_tensors(S)[1])
     if E > 0:
+        sets2 = [{proj: make_single_set(torch, synth, binding, dev, f"single_c3_{proj}", SEED + NSETS + k,
+                                        f"bench{NSETS + k}_{proj}") for proj in ("up", "down")} for k in range(NSETS)]
+        pairs = [(sets, ops), (sets2, c3_step_ops(sets2, lora, binding))]
+        host_in = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in h2d_d2h_tensors(S)[0]]
+                   for S in sets]
+        host_out = [[[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in h2d_d2h_tensors(S)[1]]
+                     for S in sets] for _ in pairs]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in pairs]
+        ev_comp = [torch.cuda.Event() for _ in pairs]
+        ev_out = [torch.cuda.Event() for _ in pairs]
+        out_pending = [False for _ in pairs]
+
+        def e2e_step(i):
+            c = i % len(pairs)
+            psets, pops = pairs[c]
+            if out_pending[c]:
+                s_in.wait_event(ev_out[c])
+            with torch.cuda.stream(s_in):
+                for k, S in enumerate(psets):
+                    for dst, src in zip(h2d_d2h_tensors(S)[0], host_in[k]):
+                        dst.copy_(src, non_blocking=True)
+                ev_in[c].record(s_in)
+            stream.wait_event(ev_in[c])
+            for _, fn, _ in pops:
+                fn(i)
+            ev_comp[c].record(stream)
+            s_out.wait_event(ev_comp[c])
+            with torch.cuda.stream(s_out):
+                for k, S in enumerate(psets):
+                    for dst, src in zip(host_out[c][k], h2d_d2h_tensors(S)[1]):
+                        dst.copy_(src, non_blocking=True)
+                ev_out[c].record(s_out)
+            out_pending[c] = True
+
         for i in range(2):
             e2e_step(i)
         torch.cuda.synchronize()
         barrier()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(stream)
+        s_in.wait_event(f0)
+        s_out.wait_event(f0)
         for i in range(E):
             e2e_step(i)
+        stream.wait_stream(s_out)
         f1.record(stream)
         torch.cuda.synchronize()
         e_ms = reduce_max(f0.elapsed_time(f1) / E, dev)
-    del host_in, host_out
+        del sets2, pairs
+    if E > 0:
+        del host_in, host_out
     assert lora.lora_device_error() == 0
 
     parts = None
@@ -668,7 +697,9 @@ def run_gb300(args, rank, world, local_rank):
                 "step_parts": step_parts, "parts": parts, "roofline": roof, "cpu_baseline": cpu,
                 "e2e": None if e_ms is None else {
                     "value": weak_scaling_value(tokens, world, e_ms), "unit": UNIT, "steps": E,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "copies": "pinned host buffers; inputs in and results out on streams of their own, "
+                              "alternate steps on two device copies of the inputs"},
                 "gpu_launches": int(launches), "clocks": sampler.summary(t_host0, t_host1)}
         print(json.dumps(line), flush=True)
 
