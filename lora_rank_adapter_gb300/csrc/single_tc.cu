@@ -413,9 +413,17 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
   uint64_t *dempty = dfull + ND;   // [ND]
   uint64_t *mdone = dempty + ND;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mdone + 1);
+  // the unit of the g-th stage of this CTA's sequence, written by the loader
+  // before it arrives on the stage's barriers (the MMA warp reads it after its
+  // B^T wait, the epilogue after its Y wait); -1 ends the sequence
+  int64_t *s_u = reinterpret_cast<int64_t *>(tmem_slot + 2);
+  constexpr int kQ = 16;   // more than the loader can run ahead of the epilogue
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t u0 = sk_begin(p.U, p.G, blockIdx.x), u1 = sk_begin(p.U, p.G, blockIdx.x + 1);
+  // the first Us units are dealt evenly (stream-K), the rest CH at a time to
+  // whichever CTA asks first: SMs stream at rates some percent apart, and the
+  // shared tail lets the fast ones take more
+  const int64_t u0 = sk_begin(p.Us, p.G, blockIdx.x), u1 = sk_begin(p.Us, p.G, blockIdx.x + 1);
   const int nl = p.nl;
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -449,17 +457,19 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
       prefetch_tmap(&tmY);
       prefetch_tmap(&tmB);
       int64_t prev = -1;
-      int hidx = 0;
-      for (int64_t u = u0; u < u1; ++u) {
+      int hidx = 0, g = 0;
+      // unit u into the stages of sequence number g; false after a timed-out wait
+      auto issue = [&](int64_t u) -> bool {
         const int64_t rb = u / nl;
         const int lc = (int)(u % nl);
-        const int g = (int)(u - u0), s = g % NS, sb = g % NBB;
-        if (g >= NS && !mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) break;
+        const int s = g % NS, sb = g % NBB;
+        if (g >= NS && !mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) return false;
+        s_u[g % kQ] = u;
         mbar_arrive_expect_tx(&full[s], C::Y_B);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
           tma_load_2d(ring + s * C::Y_B + hf * (TM * BOXC * 2), &tmY, &full[s], lc * EUC + hf * BOXC, (int)(rb * TM));
-        if (g >= NBB && !mbar_wait(&bempty[sb], ((g / NBB) & 1) ^ 1)) break;
+        if (g >= NBB && !mbar_wait(&bempty[sb], ((g / NBB) & 1) ^ 1)) return false;
         uint8_t *bt = bring + sb * C::B_B;
         mbar_arrive_expect_tx(&bfull[sb], C::B_B);
 #pragma unroll
@@ -472,11 +482,31 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
         // that a buffer still read by the previous block's MMAs delays no Y copy
         if (rb != prev) {
           const int hb = hidx % NB;
-          if (hidx >= NB && !mbar_wait(&hempty[hb], ((hidx / NB) & 1) ^ 1)) break;
+          if (hidx >= NB && !mbar_wait(&hempty[hb], ((hidx / NB) & 1) ^ 1)) return false;
           mbar_arrive_expect_tx(&hfull[hb], C::HB);
           bulk_load(hbuf + hb * C::HB, p.blob + rb * (int64_t)C::HB, C::HB, &hfull[hb]);
           prev = rb;
           ++hidx;
+        }
+        ++g;
+        return true;
+      };
+      bool ok = true;
+      for (int64_t u = u0; ok && u < u1; ++u) ok = issue(u);
+      while (ok && p.next != nullptr) {
+        const int64_t a0 = p.Us + (int64_t)atomicAdd(p.next, 1) * p.CH;
+        if (a0 >= p.U) break;
+        const int64_t a1 = a0 + p.CH < p.U ? a0 + p.CH : p.U;
+        for (int64_t u = a0; ok && u < a1; ++u) ok = issue(u);
+      }
+      if (ok) {
+        // the end of the sequence, through the barriers the MMA warp and the
+        // epilogue wait on next
+        const int s = g % NS, sb = g % NBB;
+        if (g < NS || mbar_wait(&empty[s], ((g / NS) & 1) ^ 1)) {
+          s_u[g % kQ] = -1;
+          mbar_arrive(&full[s]);
+          if (g < NBB || mbar_wait(&bempty[sb], ((g / NBB) & 1) ^ 1)) mbar_arrive(&bfull[sb]);
         }
       }
     }
@@ -484,9 +514,10 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
     if (lane == 0) {
       const uint32_t idesc = tc_idesc(TM, EUC, false, false);
       int64_t prev = -1;
-      int hidx = 0, hb = 0;
-      bool ok = true;
-      for (int64_t u = u0; ok && u < u1; ++u) {
+      int hidx = 0, hb = 0, g = 0;
+      bool ok = mbar_wait(&bfull[0], 0);
+      int64_t u = ok ? s_u[0] : -1;
+      while (ok && u >= 0) {
         const int64_t rb = u / nl;
         if (rb != prev) {
           hb = hidx % NB;
@@ -494,9 +525,8 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
           prev = rb;
           ++hidx;
         }
-        const int g = (int)(u - u0), sb = g % NBB, b = g % ND;
+        const int sb = g % NBB, b = g % ND;
         if (g >= ND && !(ok = mbar_wait(&dempty[b], ((g / ND) & 1) ^ 1))) break;
-        if (!(ok = mbar_wait(&bfull[sb], (g / NBB) & 1))) break;
         tc_fence_after();
         const uint32_t hh = smem_u32(hbuf + hb * C::HB), bb = smem_u32(bring + sb * C::B_B);
 #pragma unroll
@@ -510,7 +540,17 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
           }
         tc_commit(&dfull[b]);
         tc_commit(&bempty[sb]);
-        if (u == u1 - 1 || (u + 1) / nl != rb) tc_commit(&hempty[hb]);
+        ++g;
+        // the next unit (or the end) tells whether this row block's blob is still read
+        if (!(ok = mbar_wait(&bfull[g % NBB], (g / NBB) & 1))) break;
+        const int64_t un = s_u[g % kQ];
+        if (un < 0 || un / nl != rb) tc_commit(&hempty[hb]);
+        u = un;
+      }
+      if (ok) {
+        // the end of the sequence for the epilogue
+        const int b = g % ND;
+        if (g < ND || mbar_wait(&dempty[b], ((g / ND) & 1) ^ 1)) mbar_arrive(&dfull[b]);
       }
       tc_commit(mdone);
       mbar_wait(mdone, 0);
@@ -527,9 +567,11 @@ __global__ void __launch_bounds__(NTHR, 1) expand_kernel(const __grid_constant__
     const float scale = p.scale;
     int pend = -1;   // stage whose store may still be reading it
     if (lane == 0) prefetch_tmap(&tmYs);
-    for (int64_t u = u0; u < u1; ++u) {
-      const int g = (int)(u - u0), s = g % NS, b = g % ND;
+    for (int g = 0;; ++g) {
+      const int s = g % NS, b = g % ND;
       if (!wait_warp(&dfull[b], (g / ND) & 1) || !wait_warp(&full[s], (g / NS) & 1)) break;
+      const int64_t u = s_u[g % kQ];
+      if (u < 0) break;
       tc_fence_after();
       uint8_t *ys = ring + s * C::Y_B;
 #pragma unroll
@@ -1083,7 +1125,8 @@ lora_status_t launch_col(const void *in, int64_t ld_in, int64_t M, int64_t Cdim,
 }
 
 template <int RP>
-lora_status_t launch_expand(const uint8_t *blob, const SingleArgs &a, const CUtensorMap &tB, cudaStream_t st) {
+lora_status_t launch_expand(const uint8_t *blob, const SingleArgs &a, const CUtensorMap &tB, int *next,
+                            cudaStream_t st) {
   using Cf = ExpCfg<RP>;
   auto kern = expand_kernel<RP>;
   LORA_CUDA(ensure_smem((const void *)kern, Cf::BYTES));
@@ -1098,6 +1141,12 @@ lora_status_t launch_expand(const uint8_t *blob, const SingleArgs &a, const CUte
   p.nl = (int)nl;
   p.U = nrb * nl;
   p.G = G;
+  // the last eighth of the units (in chunks of about a thirtieth of a CTA's
+  // share) go to whichever CTA is free first
+  const bool tail = next != nullptr && p.U >= 4 * (int64_t)G;
+  p.CH = tail ? (int)std::max<int64_t>(1, std::min<int64_t>(4, p.U / (32 * (int64_t)G))) : 1;
+  p.Us = p.U - (tail ? p.U / 8 / p.CH * p.CH : 0);
+  p.next = tail ? next : nullptr;
   p.blob = blob;
   p.Y = (__nv_bfloat16 *)a.Y;
   p.ldy = a.ldy;
@@ -1144,7 +1193,8 @@ lora_status_t forward_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStr
   WsCarver carver(ws, ws_bytes);
   const void *Ac = nullptr, *Bc = nullptr;
   lora_status_t e;
-  int *cnt = take_counters(carver, ceil_div(a.M, TM), st, &e);
+  // the rows pass's tickets and the expand's claim counter
+  int *cnt = take_counters(carver, ceil_div(a.M, TM) + 1, st, &e);
   LORA_TRY(e);
   LORA_TRY(pack_tc(a, lay, carver, &Ac, &Bc, st));
   CUtensorMap tA, tB;
@@ -1153,7 +1203,7 @@ lora_status_t forward_rp(const SingleArgs &a, void *ws, size_t ws_bytes, cudaStr
   LORA_TRY((launch_rows<RP, false>(a.X, a.ldx, a.M, a.K, a.r, tA, cnt, carver, &blob, a.h, a.ldh, st)));
   if (a.L == 0) return LORA_OK;
   if (!map_bc_tc(&tB, Bc, a.L, a.r, lay.ldb, RP)) return LORA_ERR_ALIGNMENT;
-  return launch_expand<RP>(blob, a, tB, st);
+  return launch_expand<RP>(blob, a, tB, cnt + ceil_div(a.M, TM), st);
 }
 
 // dyb blob, then dX and dA; cnt holds ceil(M/128) + ceil(K/128) counters.  With
@@ -1238,7 +1288,7 @@ size_t tc_ws_bytes(int op, int64_t M, int64_t K, int64_t L, int r) {
   return by_rank(r, [&](auto rp) -> size_t {
     constexpr int RP = decltype(rp)::value;
     const size_t hb = ws_round((size_t)nrb * 2 * blob_tile(RP));
-    if (op == LORA_OP_FORWARD) return ws_round((size_t)nrb * 4) + packA + packB + ws_rows<RP>(M, K);
+    if (op == LORA_OP_FORWARD) return ws_round((size_t)(nrb + 1) * 4) + packA + packB + ws_rows<RP>(M, K);
     if (op == LORA_OP_BACKWARD_DX_DA)
       return ws_round((size_t)(nrb + nkb) * 4) + packA + packB + ws_rows<RP>(M, L) + ws_col<RP>(M, K);
     if (op == LORA_OP_BACKWARD_DB)

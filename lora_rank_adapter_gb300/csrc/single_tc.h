@@ -52,6 +52,9 @@ struct TcColArgs {
 struct TcExpArgs {
   int M, L, nl;
   int64_t U;
+  int64_t Us;                // units [0, Us) dealt evenly, [Us, U) claimed CH at a time
+  int CH;
+  int *next;                 // claim counter (zeroed before the launch), or null: no shared tail
   int G;
   const uint8_t *blob;       // hi / lo tiles of h per row block
   __nv_bfloat16 *Y;
