@@ -28,7 +28,9 @@
  *   - Strides are in ELEMENTS.  "Big" row-major operands (X, Y, dY, dX, x, y)
  *     have unit column stride; their base must be 16-byte aligned and their row
  *     stride times the element size a multiple of 16 bytes, else
- *     LORA_ERR_ALIGNMENT.  Small operands (A, B, a, b, dA, dB) take arbitrary
+ *     LORA_ERR_ALIGNMENT.  With LORA_BF16 the single-adapter extents K and L
+ *     must also be multiples of 8 (rows of Y and dX are stored in 16-byte
+ *     pieces), else LORA_ERR_ALIGNMENT.  Small operands (A, B, a, b, dA, dB) take arbitrary
  *     strides (e.g. PEFT's lora_A.weight stored r x K is A with sA_k = 1,
  *     sA_r = K).
  *   - Dtypes: LORA_BF16 = bf16 storage with fp32 accumulation, LORA_F32 = fp32

@@ -127,6 +127,9 @@ static lora_status_t check_single_common(lora_dtype_t dt, int64_t M, int64_t K, 
   if (dt != LORA_F32 && dt != LORA_BF16) return LORA_ERR_UNSUPPORTED;
   if (!size_ok(M) || !size_ok(K) || !size_ok(L) || r < 0) return LORA_ERR_INVALID_ARG;
   if (r > LORA_MAX_RANK) return LORA_ERR_UNSUPPORTED;
+  // bf16 Y and dX rows go out by tensor-copy stores, which write whole 16-byte
+  // pieces: a row ending inside one would have its neighbour elements rewritten
+  if (dt == LORA_BF16 && (K % 8 != 0 || L % 8 != 0)) return LORA_ERR_ALIGNMENT;
   return LORA_OK;
 }
 
@@ -155,7 +158,9 @@ const char *lora_status_string(lora_status_t s) {
     case LORA_OK: return "LORA_OK";
     case LORA_ERR_INVALID_ARG: return "LORA_ERR_INVALID_ARG: null pointer, negative size or inconsistent arguments";
     case LORA_ERR_UNSUPPORTED: return "LORA_ERR_UNSUPPORTED: beyond the compiled limits (rank, slices, slots, dtype)";
-    case LORA_ERR_ALIGNMENT: return "LORA_ERR_ALIGNMENT: big operand not 16-byte aligned or row stride not 16-byte";
+    case LORA_ERR_ALIGNMENT:
+      return "LORA_ERR_ALIGNMENT: big operand not 16-byte aligned, row stride not 16-byte, or a bf16 extent not "
+             "a multiple of 8";
     case LORA_ERR_WORKSPACE: return "LORA_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case LORA_ERR_CUDA: return "LORA_ERR_CUDA: a CUDA call or kernel launch failed";
     case LORA_ERR_DEVICE: return "LORA_ERR_DEVICE: a kernel flagged a device-side error";

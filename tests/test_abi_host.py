@@ -52,6 +52,8 @@ def test_forward_argument_errors(L):
     assert fwd(L, ldx=60) == 1                     # ldx < K
     assert fwd(L, ldx=68) == 3                     # row stride not a 16-byte multiple (bf16)
     assert fwd(L, dt=0, ldx=66, K=66) == 3         # fp32: 264 bytes is not a multiple of 16
+    assert fwd(L, K=60) == 3                       # bf16 K not a multiple of 8 (ldx 64 stays legal)
+    assert fwd(L, L_=60) == 3                      # bf16 L not a multiple of 8 (ldy 64 stays legal)
     # A stored K x r (not the TMA-readable layout) needs workspace for repacking
     assert fwd(L, sak=16, sar=1) == 4
     # degenerate shapes are a no-op and touch nothing (no device needed)

@@ -130,6 +130,28 @@ def test_single_bf16_many_tiles_per_cta(M, K, L, r):
     check_all(w, spec["s"], out, TOL_BF16)
 
 
+@pytest.mark.parametrize("M,K,L,r", [(12000, 256, 14200, 64), (15900, 128, 11896, 32)])
+def test_forward_shared_tail_ragged(M, K, L, r):
+    """Forwards large enough for the expand's shared tail (its last eighth of
+    (row block, 128-column chunk) units claimed two at a time by whichever CTA
+    is free first), with a ragged last row block and column chunk, chunks that
+    cross row blocks, and one and two blob buffers (r = 64, 32).  y0 = 0, so a
+    unit updated twice or not at all shows in full."""
+    spec = synth.single_spec("single_c2", M=M, K=K, L=L, r=r)
+    w = synth.make_single(spec, seed=M + L, device=DEV)
+    Al, Bl = layouts(w["A"], w["B"], "peft")
+    Y, Ybuf = padded(torch.zeros((M, L), dtype=w["X"].dtype, device=DEV), 3, 5)
+    h = torch.empty((M, r), dtype=torch.float32, device=DEV)
+    ref = O.forward(f64(w["X"]), f64(w["A"]), f64(w["B"]), np.zeros((M, L)), spec["s"])
+    for _ in range(2):   # the claim counter starts from zero on every call
+        Y.zero_()
+        lora.lora_forward_h(w["X"], Al, Bl, Y, spec["s"], h)
+        torch.cuda.synchronize()
+        assert lora.lora_device_error() == 0
+        assert rel_err(f64(Y), ref) <= TOL_BF16
+        assert untouched(Ybuf, M, L)
+
+
 @pytest.mark.parametrize("M,K,L,r", [(3, 24, 40, 3), (130, 200, 72, 16), (65, 96, 128, 33)])
 def test_single_bf16_strided_small_operands(M, K, L, r):
     spec = synth.single_spec("single_c2", M=M, K=K, L=L, r=r)
