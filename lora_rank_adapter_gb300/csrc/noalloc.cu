@@ -112,6 +112,7 @@ extern "C" lora_status_t lora_backward_db_noalloc(lora_dtype_t dtype, int64_t M,
   if (M < 0 || K < 0 || L < 0 || r < 0 || M >= kMaxDim || K >= kMaxDim || L >= kMaxDim)
     return LORA_ERR_INVALID_ARG;
   if (r > LORA_MAX_RANK) return LORA_ERR_UNSUPPORTED;
+  if (dtype == LORA_BF16 && (K % 8 != 0 || L % 8 != 0)) return LORA_ERR_ALIGNMENT;
   const size_t need = lora_workspace_size(LORA_OP_BACKWARD_DB, dtype, M, K, L, r, 0);
   if (need > LORA_DB_NOALLOC_SCRATCH_BYTES) return LORA_ERR_WORKSPACE;
   void *ws = nullptr;

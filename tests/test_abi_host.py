@@ -84,6 +84,28 @@ def test_backward_argument_errors(L):
     assert db() == 4
 
 
+def test_bf16_extents_multiple_of_8(L):
+    """bf16 single-adapter calls with K or L off a multiple of 8 return
+    LORA_ERR_ALIGNMENT before anything else is looked at (rows of Y and dX are
+    stored in 16-byte pieces); fp32 keeps any extent."""
+    for K, Lc in ((60, 64), (64, 60)):
+        assert L.lora_backward_dx_da(1, 64, K, Lc, 16, FAKE, 64, FAKE, 64, FAKE, 1, 64, FAKE, 1, 16, 1.0,
+                                     FAKE, 64, FAKE, 16, 1, NULL, 0, S0) == 3
+        assert L.lora_backward_db(1, 64, K, Lc, 16, FAKE, 64, FAKE, 1, 64, FAKE, 64, 1.0, FAKE, 64, 1,
+                                  NULL, 0, S0) == 3
+        assert L.lora_forward_h(1, 64, K, Lc, 16, FAKE, 64, FAKE, 1, 64, FAKE, 1, 16, FAKE, 64, 1.0, FAKE, 16,
+                                NULL, 0, S0) == 3
+        assert L.lora_backward(1, 64, K, Lc, 16, FAKE, 64, FAKE, 64, FAKE, 1, 64, FAKE, 1, 16, FAKE, 16, 1.0,
+                               FAKE, 64, FAKE, 16, 1, FAKE, 64, 1, NULL, 0, S0) == 3
+        assert L.lora_backward_ex(1, 64, K, Lc, 16, FAKE, 64, FAKE, 64, FAKE, 1, 64, FAKE, 1, 16, FAKE, 16, 1.0,
+                                  FAKE, 64, FAKE, 16, 1, FAKE, 64, 1, 0, NULL, 0, S0) == 3
+        assert L.lora_backward_db_noalloc(1, 64, K, Lc, 16, FAKE, 64, FAKE, 1, 64, FAKE, 64, 1.0, FAKE, 64, 1,
+                                          S0) == 3
+    # fp32: the same extents pass the checks (and then want their workspace)
+    assert L.lora_backward_dx_da(0, 64, 60, 60, 16, FAKE, 64, FAKE, 64, FAKE, 1, 64, FAKE, 1, 16, 1.0,
+                                 FAKE, 64, FAKE, 16, 1, NULL, 0, S0) == 4
+
+
 def test_fused_argument_errors(L):
     fh = lambda **k: L.lora_forward_h(1, k.get("M", 64), 64, 64, 16, FAKE, 64, FAKE, 1, 64, FAKE, 1, 16, FAKE, 64,
                                       1.0, k.get("h", FAKE), k.get("ldh", 16), NULL, 0, S0)
